@@ -1,0 +1,17 @@
+"""CPU oracle for the routing + dispatch + grouped-GEMM path.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only users.  The product library never imports it.
+"""
+from .oracle import (  # noqa: F401
+    build_oracle,
+    topk,
+    histogram,
+    permutation,
+    rank_base,
+    gather,
+    grouped_gemm,
+    gemm_entry,
+    expert_of_row,
+    route,
+)

@@ -1,0 +1,199 @@
+/*
+ * Plain CPU oracle for the routing + dispatch + per-expert grouped GEMM path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA path.
+ *
+ * What it follows.  The articles on mKernel ("Conozca mKernel ..." on
+ * 7minutos.es and its Arabic twin on k7ail.com), table "the five fused
+ * kernels", row "MoE Dispatch + GEMM", describe the operation in one
+ * sentence: route MoE tokens to their expert ranks (all-to-all) and run the
+ * per-expert grouped GEMM in the same kernel, computing on tokens as soon as
+ * they land.  The pages fix nothing finer than that.  Every step below is the
+ * plain definition under the readings this library adopts (selection on the
+ * logits, lower expert index wins ties, softmax over all experts, stable order
+ * by token then slot inside each expert, rank-major expert-contiguous receive
+ * rows, fp64 accumulation in ascending k order).
+ *
+ * Floating point: every sum is a plain left-to-right fp64 sum.  Build with
+ * -ffp-contract=off so that no compiler fuses a product into an add.
+ *
+ * bf16 values are passed as their 16-bit patterns (uint16_t); a bf16 pattern
+ * b is the fp32 number whose bit pattern is b << 16.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Step A1: top-k over the softmax of each token's router logits.
+ *
+ * Selection is made on the logits themselves (softmax is strictly increasing,
+ * so the order is the same).  The j-th pick is the largest logit not yet
+ * picked; between equal logits the lower expert index is picked first.  The
+ * comparison is the float comparison, so -0.0 and +0.0 are equal.
+ * Logits must be finite; the function returns -1 on a NaN.
+ *
+ * topk_w[t*k+j] = exp(L[t][e_j] - m_t) / sum_e exp(L[t][e] - m_t), with m_t
+ * the row maximum: the softmax over all E experts, in fp64, with no
+ * renormalisation over the k picks.
+ */
+ORACLE_API int oracle_topk(const float* logits, int T, int E, int k,
+                           int32_t* topk_idx, double* topk_w) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return -2;
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!taken) return -3;
+    for (int t = 0; t < T; ++t) {
+        const float* L = logits + (size_t)t * E;
+        for (int e = 0; e < E; ++e)
+            if (isnan(L[e])) { free(taken); return -1; }
+        memset(taken, 0, (size_t)E);
+        double m = (double)L[0];
+        for (int e = 1; e < E; ++e)
+            if ((double)L[e] > m) m = (double)L[e];
+        double s = 0.0;
+        for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || L[e] > L[best]) best = e;  /* strict: ties keep the lower index */
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+            topk_w[(size_t)t * k + j] = exp((double)L[best] - m) / s;
+        }
+    }
+    free(taken);
+    return 0;
+}
+
+/*
+ * Step A2: per-expert histogram and its exclusive prefix sum.
+ * counts[e] = number of (t, j) with topk_idx[t*k+j] == e;
+ * offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e].
+ * Returns -1 if an index is outside [0, E).
+ */
+ORACLE_API int oracle_histogram(const int32_t* topk_idx, int T, int k, int E,
+                                int32_t* counts, int32_t* offsets) {
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (long s = 0; s < (long)T * k; ++s) {
+        int e = topk_idx[s];
+        if (e < 0 || e >= E) return -1;
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    return 0;
+}
+
+/*
+ * Step A3: the stable permutation.  Destination rows are filled expert by
+ * expert (ascending); inside one expert, by token (ascending) and then by
+ * slot (ascending).  perm[row] = source slot t*k+j, dest[t*k+j] = row.
+ */
+ORACLE_API int oracle_permutation(const int32_t* topk_idx, int T, int k, int E,
+                                  int32_t* perm, int32_t* dest) {
+    long pos = 0;
+    for (int e = 0; e < E; ++e)
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j)
+                if (topk_idx[(size_t)t * k + j] == e) {
+                    perm[pos] = t * k + j;
+                    dest[(size_t)t * k + j] = (int32_t)pos;
+                    ++pos;
+                }
+    return pos == (long)T * k ? 0 : -1;
+}
+
+/*
+ * Receive-buffer split over R simulated expert ranks.  Rank r owns experts
+ * [r*E/R, (r+1)*E/R); its rows are the global destination rows
+ * [offsets[r*E/R], offsets[(r+1)*E/R]) in the same order, so row i of rank r's
+ * buffer is global destination row rank_base[r] + i.  rank_base has R+1
+ * entries; rank_base[R] = T*k.
+ */
+ORACLE_API int oracle_rank_base(const int32_t* offsets, int E, int R, int32_t* rank_base) {
+    if (R < 1 || E % R != 0) return -1;
+    for (int r = 0; r <= R; ++r) rank_base[r] = offsets[(size_t)r * (E / R)];
+    return 0;
+}
+
+/*
+ * Step A4: dispatch.  Destination row `row` receives a bit copy of the
+ * token row x[perm[row] / k].  Rows are written in global destination order
+ * (rank 0's rows first); the caller slices per rank with oracle_rank_base.
+ */
+ORACLE_API void oracle_gather(const uint16_t* x, int T, int d, int k,
+                              const int32_t* perm, long S, uint16_t* rows) {
+    (void)T;
+    for (long row = 0; row < S; ++row) {
+        int t = perm[row] / k;
+        for (int i = 0; i < d; ++i) rows[(size_t)row * d + i] = x[(size_t)t * d + i];
+    }
+}
+
+/*
+ * Step A5: per-expert grouped GEMM on the destination rows.
+ * For each expert e and each row in its segment [offsets[e], offsets[e+1]):
+ *   Y[row][n] = sum_{i=0}^{d-1} rows[row][i] * W[e][i][n]
+ * summed in fp64, i ascending.  W is [E][d][N] (N contiguous).
+ * The loop visits i in the outer position with one fp64 accumulator per
+ * output column; each Y element still sees its terms in ascending i.
+ */
+ORACLE_API int oracle_grouped_gemm(const uint16_t* rows, const uint16_t* W,
+                                   const int32_t* offsets, int E, int d, int N,
+                                   double* Y) {
+    double* acc = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!acc) return -3;
+    for (int e = 0; e < E; ++e) {
+        const uint16_t* We = W + (size_t)e * d * N;
+        for (long row = offsets[e]; row < offsets[e + 1]; ++row) {
+            for (int n = 0; n < N; ++n) acc[n] = 0.0;
+            for (int i = 0; i < d; ++i) {
+                double a = bf16_to_double(rows[(size_t)row * d + i]);
+                const uint16_t* wrow = We + (size_t)i * N;
+                for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(wrow[n]);
+            }
+            for (int n = 0; n < N; ++n) Y[(size_t)row * N + n] = acc[n];
+        }
+    }
+    free(acc);
+    return 0;
+}
+
+/*
+ * One element of step A5, for sampled checks at full size:
+ *   sum_{i<d} row[i] * We[i][n]   (fp64, i ascending)
+ * `row` is one destination row (d values), `We` one expert's [d][N] matrix.
+ */
+ORACLE_API double oracle_gemm_entry(const uint16_t* row, const uint16_t* We,
+                                    int d, int N, int n) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i)
+        acc += bf16_to_double(row[i]) * bf16_to_double(We[(size_t)i * N + n]);
+    return acc;
+}
+
+/*
+ * Expert that owns destination row `row`: the e with
+ * offsets[e] <= row < offsets[e+1] (a linear scan; empty experts are skipped
+ * because their segment is empty).
+ */
+ORACLE_API int oracle_expert_of_row(const int32_t* offsets, int E, long row) {
+    for (int e = 0; e < E; ++e)
+        if (offsets[e] <= row && row < offsets[e + 1]) return e;
+    return -1;
+}

@@ -1,0 +1,160 @@
+"""ctypes front end of the plain C oracle (``moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Each function below hands numpy arrays to one C
+function of the oracle and returns numpy arrays; no arithmetic of the method
+happens here.  See ``moe_oracle.c`` for the definition each step follows.
+
+bf16 tensors travel as their uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so next to it (gcc, no FMA contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+             "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build_oracle())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_long
+            lib.oracle_topk.argtypes = [P, I, I, I, P, P]
+            lib.oracle_topk.restype = I
+            lib.oracle_histogram.argtypes = [P, I, I, I, P, P]
+            lib.oracle_histogram.restype = I
+            lib.oracle_permutation.argtypes = [P, I, I, I, P, P]
+            lib.oracle_permutation.restype = I
+            lib.oracle_rank_base.argtypes = [P, I, I, P]
+            lib.oracle_rank_base.restype = I
+            lib.oracle_gather.argtypes = [P, I, I, I, P, L, P]
+            lib.oracle_gather.restype = None
+            lib.oracle_grouped_gemm.argtypes = [P, P, P, I, I, I, P]
+            lib.oracle_grouped_gemm.restype = I
+            lib.oracle_gemm_entry.argtypes = [P, P, I, I, I]
+            lib.oracle_gemm_entry.restype = ctypes.c_double
+            lib.oracle_expert_of_row.argtypes = [P, I, L]
+            lib.oracle_expert_of_row.restype = I
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def topk(logits: np.ndarray, k: int):
+    """Step A1 -> (topk_idx int32 [T,k], topk_w float64 [T,k])."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = L.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    rc = _load().oracle_topk(_p(L), T, E, k, _p(idx), _p(w))
+    if rc != 0:
+        raise ValueError(f"oracle_topk failed ({rc})")
+    return idx, w
+
+
+def histogram(topk_idx: np.ndarray, E: int):
+    """Step A2 -> (counts int32 [E], offsets int32 [E+1])."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    rc = _load().oracle_histogram(_p(idx), T, k, E, _p(counts), _p(offsets))
+    if rc != 0:
+        raise ValueError("expert index out of range")
+    return counts, offsets
+
+
+def permutation(topk_idx: np.ndarray, E: int):
+    """Step A3 -> (perm int32 [T*k], dest int32 [T*k])."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    perm = np.empty(T * k, np.int32)
+    dest = np.empty(T * k, np.int32)
+    rc = _load().oracle_permutation(_p(idx), T, k, E, _p(perm), _p(dest))
+    if rc != 0:
+        raise ValueError("permutation incomplete")
+    return perm, dest
+
+
+def rank_base(offsets: np.ndarray, R: int):
+    """First global destination row of each simulated rank; [R+1] int32."""
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    E = off.shape[0] - 1
+    out = np.empty(R + 1, np.int32)
+    if _load().oracle_rank_base(_p(off), E, R, _p(out)) != 0:
+        raise ValueError("R must divide E")
+    return out
+
+
+def gather(x_bits: np.ndarray, perm: np.ndarray, k: int):
+    """Step A4: destination rows (uint16 bf16 bits) in global destination order."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, d = x.shape
+    pm = np.ascontiguousarray(perm, dtype=np.int32)
+    S = pm.shape[0]
+    rows = np.empty((S, d), np.uint16)
+    _load().oracle_gather(_p(x), T, d, k, _p(pm), S, _p(rows))
+    return rows
+
+
+def grouped_gemm(rows_bits: np.ndarray, W_bits: np.ndarray, offsets: np.ndarray):
+    """Step A5 on every destination row -> Y float64 [S, N]."""
+    rows = np.ascontiguousarray(rows_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    E, d, N = W.shape
+    S = rows.shape[0]
+    Y = np.empty((S, N), np.float64)
+    if _load().oracle_grouped_gemm(_p(rows), _p(W), _p(off), E, d, N, _p(Y)) != 0:
+        raise MemoryError
+    return Y
+
+
+def gemm_entry(row_bits: np.ndarray, We_bits: np.ndarray, n: int) -> float:
+    """One element of step A5: row . We[:, n] in fp64."""
+    row = np.ascontiguousarray(row_bits, dtype=np.uint16)
+    We = np.ascontiguousarray(We_bits, dtype=np.uint16)
+    d, N = We.shape
+    assert row.shape == (d,)
+    return float(_load().oracle_gemm_entry(_p(row), _p(We), d, N, int(n)))
+
+
+def expert_of_row(offsets: np.ndarray, row: int) -> int:
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    return int(_load().oracle_expert_of_row(_p(off), off.shape[0] - 1, int(row)))
+
+
+def route(logits: np.ndarray, k: int):
+    """Steps A1-A3 chained: returns a dict of the oracle's routing outputs."""
+    E = logits.shape[1]
+    idx, w = topk(logits, k)
+    counts, offsets = histogram(idx, E)
+    perm, dest = permutation(idx, E)
+    return {"topk_idx": idx, "topk_w": w, "counts": counts, "offsets": offsets,
+            "perm": perm, "dest": dest}

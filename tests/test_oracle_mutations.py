@@ -1,0 +1,88 @@
+"""Plant plausible mistakes in a private copy of the oracle and check that the
+pins catch each one.  Everything here runs on the CPU; the real oracle is
+never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTATIONS = {
+    # ties go to the higher expert index
+    "tie_rule": ("if (best < 0 || L[e] > L[best]) best = e;",
+                 "if (best < 0 || L[e] >= L[best]) best = e;"),
+    # destination order by slot before token
+    "perm_order": ("for (int t = 0; t < T; ++t)\n            for (int j = 0; j < k; ++j)\n                if (topk_idx",
+                   "for (int j = 0; j < k; ++j)\n            for (int t = 0; t < T; ++t)\n                if (topk_idx"),
+    # softmax denominator drops one term
+    "softmax_sum": ("for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);",
+                    "for (int e = 1; e < E; ++e) s += exp((double)L[e] - m);"),
+    # transposed weight operand
+    "gemm_transpose": ("const uint16_t* wrow = We + (size_t)i * N;\n                for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(wrow[n]);",
+                       "for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(We[((size_t)n * d + i) % ((size_t)d * N)]);"),
+    # gather by slot index instead of token index
+    "gather_index": ("int t = perm[row] / k;", "int t = perm[row] % T;"),
+    # histogram off by one in the prefix sum
+    "prefix": ("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    before, after = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, name
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(before, after))
+    so = tmp_path / f"{name}.so"
+    subprocess.check_call(["gcc", "-O1", "-ffp-contract=off", "-fPIC", "-shared", "-o", str(so), str(path), "-lm"])
+    return so
+
+
+def _swap_lib(oracle_mod, so):
+    import oracle.oracle as o
+    o._load()
+    saved = o._lib
+    o._lib = None
+    real = o._LIB_PATH
+    o._LIB_PATH = str(so)
+    build = o.build_oracle
+    o.build_oracle = lambda force=False: str(so)
+    try:
+        o._load()
+    finally:
+        o._LIB_PATH = real
+        o.build_oracle = build
+    return saved
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(tmp_path, oracle_mod, name):
+    import oracle.oracle as o
+    import tests.test_oracle_pins as pins
+    so = _build_mutant(tmp_path, name)
+    saved = _swap_lib(oracle_mod, so)
+    try:
+        checks = [
+            lambda: pins.test_handworked_example(o),
+            *[(lambda s=s: pins.test_topk_matches_full_sort(o, s)) for s in range(6)],
+            lambda: pins.test_topk_special_cases(o),
+            lambda: pins.test_gate_weight_two_experts_is_logistic(o),
+            *[(lambda s=s: pins.test_histogram_and_permutation_brute_force(o, s)) for s in range(4)],
+            lambda: pins.test_gather_is_fancy_index(o),
+            lambda: pins.test_gemm_single_expert_is_plain_matmul(o),
+            lambda: pins.test_gemm_uses_each_rows_own_expert(o),
+        ]
+        caught = 0
+        for c in checks:
+            try:
+                c()
+            except (AssertionError, ValueError):
+                caught += 1
+        assert caught > 0, f"mutation {name} passed every pin"
+    finally:
+        o._lib = saved

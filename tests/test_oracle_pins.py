@@ -1,0 +1,255 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks one step of the oracle against an independent statement of
+what the step must produce: a hand-worked example, a brute-force computation
+by a different algorithm, a closed form, an invariant, or a special case that
+reduces to a library routine.  None of these calls the CUDA path.
+"""
+import collections
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _bf16_bits_from_f32(a: np.ndarray) -> np.ndarray:
+    """Round fp32 -> bf16 bits with round-to-nearest-even (test-side helper)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u >> 16) & 1) + 0x7FFF
+    return ((u + r) >> 16).astype(np.uint16)
+
+
+def _bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _read_golden(name):
+    data = {}
+    logits = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "logits":
+                logits[int(vals[0])] = [float(v) for v in vals[1:]]
+            elif key in ("T", "E", "k"):
+                data[key] = int(vals[0])
+            else:
+                data[key] = [int(v) for v in vals]
+    data["logits"] = np.array([logits[t] for t in range(data["T"])], np.float32)
+    return data
+
+
+# ---------------------------------------------------------------- A1 .. A3
+
+def test_handworked_example(oracle_mod):
+    g = _read_golden("route_handworked.txt")
+    r = oracle_mod.route(g["logits"], g["k"])
+    assert r["topk_idx"].ravel().tolist() == g["topk_idx"]
+    assert r["counts"].tolist() == g["counts"]
+    assert r["offsets"].tolist() == g["offsets"]
+    assert r["perm"].tolist() == g["perm"]
+    assert r["dest"].tolist() == g["dest"]
+
+
+def _random_logits(rng, T, E, coarse):
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    if coarse:  # a coarse grid makes exact ties common; include signed zeros
+        L = np.round(L * 2.0).astype(np.float32) / np.float32(2.0)
+        neg0 = rng.random((T, E)) < 0.1
+        L[neg0 & (L == 0)] = np.float32(-0.0)
+    return L
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_matches_full_sort(oracle_mod, seed):
+    """Brute force: a full sort of (−logit, index) per token, first k entries."""
+    rng = np.random.default_rng(seed)
+    T, E = 40, int(rng.integers(1, 13))
+    k = int(rng.integers(1, E + 1))
+    L = _random_logits(rng, T, E, coarse=seed % 2 == 0)
+    idx, _ = oracle_mod.topk(L, k)
+    for t in range(T):
+        # Python's float compare treats -0.0 == 0.0, as the definition asks
+        want = [e for _, e in sorted((-float(L[t, e]), e) for e in range(E))][:k]
+        assert idx[t].tolist() == want
+
+
+def test_topk_invariants(oracle_mod):
+    rng = np.random.default_rng(11)
+    T, E, k = 300, 64, 6
+    L = _random_logits(rng, T, E, coarse=True)
+    idx, _ = oracle_mod.topk(L, k)
+    for t in range(T):
+        chosen = set(idx[t].tolist())
+        assert len(chosen) == k
+        lo = min(L[t, e] for e in chosen)
+        assert all(L[t, e] <= lo for e in range(E) if e not in chosen)
+        # slots are in non-increasing logit order
+        assert all(L[t, idx[t, j]] >= L[t, idx[t, j + 1]] for j in range(k - 1))
+
+
+def test_topk_special_cases(oracle_mod):
+    # all logits equal -> experts 0..k-1 and uniform gate weights 1/E
+    L = np.full((3, 10), 0.37, np.float32)
+    idx, w = oracle_mod.topk(L, 4)
+    assert (idx == np.arange(4)).all()
+    assert np.allclose(w, 0.1, rtol=0, atol=1e-15)
+    # k == E -> every expert, sorted by logit, and the weights sum to one
+    rng = np.random.default_rng(3)
+    L = rng.standard_normal((20, 7)).astype(np.float32)
+    idx, w = oracle_mod.topk(L, 7)
+    assert (np.sort(idx, axis=1) == np.arange(7)).all()
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    # E == 1
+    idx, w = oracle_mod.topk(np.array([[5.0], [-3.0]], np.float32), 1)
+    assert idx.ravel().tolist() == [0, 0] and np.all(w == 1.0)
+
+
+def test_gate_weight_two_experts_is_logistic(oracle_mod):
+    """With E = 2 the softmax weight of the winner is the logistic 1/(1+e^-(a-b))."""
+    a = np.linspace(-4, 4, 17, dtype=np.float32)
+    L = np.stack([a, np.zeros_like(a)], axis=1)
+    idx, w = oracle_mod.topk(L, 1)
+    for t in range(len(a)):
+        diff = abs(float(a[t]))
+        assert w[t, 0] == pytest.approx(1.0 / (1.0 + math.exp(-diff)), abs=1e-15)
+
+
+def test_topk_rejects_nan(oracle_mod):
+    L = np.array([[0.0, np.nan, 1.0]], np.float32)
+    with pytest.raises(ValueError):
+        oracle_mod.topk(L, 1)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_histogram_and_permutation_brute_force(oracle_mod, seed):
+    rng = np.random.default_rng(100 + seed)
+    T, E = int(rng.integers(1, 50)), int(rng.integers(1, 17))
+    k = int(rng.integers(1, E + 1))
+    L = _random_logits(rng, T, E, coarse=True)
+    r = oracle_mod.route(L, k)
+    idx = r["topk_idx"]
+    cnt = collections.Counter(idx.ravel().tolist())
+    assert r["counts"].tolist() == [cnt.get(e, 0) for e in range(E)]
+    assert r["offsets"].tolist() == [0] + list(itertools.accumulate(cnt.get(e, 0) for e in range(E)))
+    assert int(r["counts"].sum()) == T * k
+    # the destination order is the sort of (expert, token, slot) triples
+    triples = sorted((int(idx[t, j]), t, j) for t in range(T) for j in range(k))
+    assert r["perm"].tolist() == [t * k + j for _, t, j in triples]
+    # bijection and inverse
+    assert sorted(r["perm"].tolist()) == list(range(T * k))
+    assert (r["dest"][r["perm"]] == np.arange(T * k)).all()
+    assert (r["perm"][r["dest"]] == np.arange(T * k)).all()
+    # inside each expert segment, tokens ascend
+    for e in range(E):
+        seg = r["perm"][r["offsets"][e]:r["offsets"][e + 1]] // k
+        assert (np.diff(seg) > 0).all()
+
+
+def test_all_tokens_on_one_expert(oracle_mod):
+    T, E, k = 33, 5, 1
+    L = np.zeros((T, E), np.float32)
+    L[:, 3] = 1.0
+    r = oracle_mod.route(L, k)
+    assert r["counts"].tolist() == [0, 0, 0, T, 0]
+    assert r["offsets"].tolist() == [0, 0, 0, 0, T, T]
+    assert r["perm"].tolist() == list(range(T))
+
+
+def test_rank_base(oracle_mod):
+    off = np.array([0, 2, 6, 7, 8], np.int32)
+    assert oracle_mod.rank_base(off, 2).tolist() == [0, 6, 8]
+    assert oracle_mod.rank_base(off, 4).tolist() == [0, 2, 6, 7, 8]
+    assert oracle_mod.rank_base(off, 1).tolist() == [0, 8]
+    with pytest.raises(ValueError):
+        oracle_mod.rank_base(off, 3)
+
+
+# ---------------------------------------------------------------- A4
+
+def test_gather_is_fancy_index(oracle_mod):
+    rng = np.random.default_rng(5)
+    T, d, E, k = 37, 24, 6, 3
+    x = rng.integers(0, 65536, size=(T, d), dtype=np.uint16)
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    r = oracle_mod.route(L, k)
+    rows = oracle_mod.gather(x, r["perm"], k)
+    assert np.array_equal(rows, x[r["perm"] // k])
+
+
+# ---------------------------------------------------------------- A5
+
+def test_gemm_single_expert_is_plain_matmul(oracle_mod):
+    """E = 1, k = 1: the grouped GEMM is one plain GEMM (numpy fp64 as cross-check)."""
+    rng = np.random.default_rng(7)
+    S, d, N = 19, 48, 40
+    a = _bf16_bits_from_f32(rng.standard_normal((S, d)).astype(np.float32))
+    W = _bf16_bits_from_f32((rng.standard_normal((1, d, N)) / np.sqrt(d)).astype(np.float32))
+    off = np.array([0, S], np.int32)
+    Y = oracle_mod.grouped_gemm(a, W, off)
+    ref = _bits_to_f64(a) @ _bits_to_f64(W[0])
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_one_hot_weights_copy_rows(oracle_mod):
+    """W_e = identity columns: Y equals the destination rows exactly."""
+    rng = np.random.default_rng(8)
+    S, d, E = 12, 16, 3
+    rows = _bf16_bits_from_f32(rng.standard_normal((S, d)).astype(np.float32))
+    eye = _bf16_bits_from_f32(np.eye(d, dtype=np.float32))
+    W = np.stack([eye] * E)
+    off = np.array([0, 5, 5, S], np.int32)  # expert 1 empty
+    Y = oracle_mod.grouped_gemm(rows, W, off)
+    assert np.array_equal(Y, _bits_to_f64(rows))
+
+
+def test_gemm_uses_each_rows_own_expert(oracle_mod):
+    """Rows in expert e's segment see W_e and no other: compare per segment."""
+    rng = np.random.default_rng(9)
+    d, N, E = 32, 24, 4
+    off = np.array([0, 3, 3, 10, 14], np.int32)
+    S = int(off[-1])
+    rows = _bf16_bits_from_f32(rng.standard_normal((S, d)).astype(np.float32))
+    W = _bf16_bits_from_f32((rng.standard_normal((E, d, N)) / np.sqrt(d)).astype(np.float32))
+    Y = oracle_mod.grouped_gemm(rows, W, off)
+    for e in range(E):
+        seg = slice(off[e], off[e + 1])
+        ref = _bits_to_f64(rows[seg]) @ _bits_to_f64(W[e])
+        assert np.allclose(Y[seg], ref, rtol=1e-12, atol=1e-12)
+        for row in range(off[e], off[e + 1]):
+            assert oracle_mod.expert_of_row(off, row) == e
+    # the single-entry helper agrees bit for bit with the full GEMM
+    for row, n in [(0, 0), (5, 7), (13, 23)]:
+        e = oracle_mod.expert_of_row(off, row)
+        assert oracle_mod.gemm_entry(rows[row], W[e], n) == Y[row, n]
+
+
+def test_gemm_within_fp64_summation_bound(oracle_mod):
+    """Exact rational re-sum: |fl(sum) - sum| <= gamma_{d-1} * sum |terms|.
+
+    bf16 x bf16 products are exact in fp64 (8-bit significands), so the only
+    error is the d-1 additions: gamma_n = n u / (1 - n u), u = 2^-53.
+    """
+    rng = np.random.default_rng(10)
+    S, d, N = 4, 64, 6
+    rows = _bf16_bits_from_f32(rng.standard_normal((S, d)).astype(np.float32) * 3)
+    W = _bf16_bits_from_f32(rng.standard_normal((1, d, N)).astype(np.float32))
+    Y = oracle_mod.grouped_gemm(rows, W, np.array([0, S], np.int32))
+    a = _bits_to_f64(rows)
+    w = _bits_to_f64(W[0])
+    u = 2.0 ** -53
+    gamma = (d - 1) * u / (1 - (d - 1) * u)
+    for i in range(S):
+        for n in range(N):
+            terms = [Fraction(float(a[i, q])) * Fraction(float(w[q, n])) for q in range(d)]
+            exact = sum(terms, Fraction(0))
+            bound = gamma * float(sum(abs(t) for t in terms))
+            assert abs(Fraction(Y[i, n]) - exact) <= Fraction(bound)

@@ -1,0 +1,46 @@
+"""The seeded input generator: determinism, shapes and the load patterns each
+workload promises (checked through the oracle's routing)."""
+import numpy as np
+import torch
+
+from moe_token_dispatch_route_gb300 import workloads as wl
+
+
+def test_deterministic_and_shaped():
+    w = wl.WORKLOADS["tiny"]
+    a = wl.make_inputs(w, seed=0)
+    b = wl.make_inputs(w, seed=0)
+    c = wl.make_inputs(w, seed=1)
+    for key in ("x", "W_r", "logits", "W"):
+        assert torch.equal(a[key], b[key])
+    assert not torch.equal(a["x"], c["x"])
+    assert a["x"].shape == (256, 512) and a["x"].dtype == torch.bfloat16
+    assert a["W"].shape == (8, 512, 1024) and a["W"].dtype == torch.bfloat16
+    assert a["logits"].shape == (256, 8) and a["logits"].dtype == torch.float32
+    assert torch.isfinite(a["logits"]).all()
+    # logits ~ N(0, 1) by construction (x ~ N(0,1), W_r ~ N(0, 1/d))
+    assert 0.8 < float(a["logits"].std()) < 1.2
+    assert 0.9 < float(a["x"].float().std()) < 1.1
+
+
+def test_decode_hot_experts_in_every_token(oracle_mod):
+    w = wl.WORKLOADS["decode"]
+    inp = wl.make_inputs(w, seed=0, with_weights=False)
+    r = oracle_mod.route(inp["logits"].numpy(), w.k)
+    hot = wl.hot_experts(w, 0)
+    for t in range(w.T):
+        assert set(hot) <= set(r["topk_idx"][t].tolist())
+    assert all(int(r["counts"][e]) == w.T for e in hot)
+    # exactly half the routing mass on the four hot experts at k = 8
+    assert sum(int(r["counts"][e]) for e in hot) * 2 == w.S
+
+
+def test_finegrained_has_empty_experts_and_skew(oracle_mod):
+    w = wl.WORKLOADS["finegrained"]
+    inp = wl.make_inputs(w, seed=0, with_weights=False)
+    r = oracle_mod.route(inp["logits"].numpy(), w.k)
+    counts = r["counts"]
+    assert (counts == 0).sum() >= 4
+    assert int(counts.sum()) == w.S
+    srt = np.sort(counts)[::-1]
+    assert srt[0] > 4 * np.median(counts)   # skewed, not uniform
