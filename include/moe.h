@@ -1,0 +1,193 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE routing + dispatch + grouped-GEMM
+ * library (libmoe_gb300.so).
+ *
+ * The operation is the "MoE Dispatch + GEMM" fused kernel of mKernel, as the
+ * articles "Conozca mKernel: una biblioteca de nucleo fusionado ..."
+ * (7minutos.es) and its Arabic twin (k7ail.com) describe it in their table of
+ * the five fused kernels, row "MoE Dispatch + GEMM": route MoE tokens to
+ * their expert ranks (an all-to-all), and run the per-expert grouped GEMM in
+ * the same kernel, on tokens as soon as they land, with no round trip through
+ * a staging buffer.  The same articles, section on the design properties,
+ * describe the kernel as persistent, with CTAs that assign themselves roles
+ * and a per-shape number of SMs per role.  On one GPU the all-to-all becomes
+ * a scatter into R simulated per-rank receive buffers in local HBM.
+ *
+ * Notation: T tokens, d hidden width (GEMM K), E experts, k experts per
+ * token, N expert output width, R simulated expert ranks, S = T*k routed
+ * slots.  bf16 tensors are passed as uint16_t bit patterns.
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller allocates and owns every device buffer and the
+ *    stream.  The library owns only the host-side plan object.  No call
+ *    allocates device memory, synchronises the host, or copies device data
+ *    to the host, except moe_read_status (documented there).
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Calls are asynchronous and stream-ordered.  Calls that
+ *    share one workspace must be ordered on one stream; overlapping them on
+ *    the GPU is a race.
+ *  - Alignment: x, W, Y and the receive buffers 16-byte aligned; int32 and
+ *    fp32 arrays 4-byte aligned; the workspace 256-byte aligned.  All rows
+ *    are dense (row stride = width).  A misaligned pointer is
+ *    MOE_ERR_INVALID_ARG (MOE_ERR_WORKSPACE for the workspace).
+ *  - Errors: argument errors are returned synchronously, before any launch,
+ *    and leave every buffer untouched.  Errors found on the device (a bounded
+ *    wait that gave up, a receive buffer overflow) are written into the
+ *    caller's `dev_status` buffer and read later with moe_read_status.  No
+ *    kernel traps.
+ *  - Shape limits: 1 <= E <= 1024; 1 <= k <= min(E, 32); 0 <= T; T*k < 2^31;
+ *    d % 64 == 0 and 64 <= d <= 65536; N % 16 == 0 and 16 <= N; E % R == 0
+ *    and 1 <= R <= 32.  Outside them: MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad field   */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid arguments outside this build's shape limits    */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or misaligned                      */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (or no device)     */
+    MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait for a ready flag gave up      */
+    MOE_ERR_CAPACITY = 6,     /* device: a rank's receive buffer is too small         */
+    MOE_ERR_DEVICE = 7        /* device: an internal pipeline wait gave up            */
+} moe_status_t;
+
+/* Opaque host-side plan: shape, tile configuration and role split. */
+typedef struct moe_plan_s* moe_plan_t;
+
+typedef struct moe_shape {
+    int32_t T;                  /* tokens                                               */
+    int32_t d;                  /* hidden width = GEMM reduction length                */
+    int32_t E;                  /* experts                                              */
+    int32_t k;                  /* experts per token                                    */
+    int32_t N;                  /* expert output width                                  */
+    int32_t num_ranks;          /* R simulated expert ranks; 0 means 1                  */
+    int32_t rank_capacity_rows; /* rows in each rank's receive buffer; 0 means T*k      */
+    int32_t tile_n;             /* GEMM tile width: 0 = auto, else 128 or 256           */
+    int32_t producer_ctas;      /* CTAs that start in the scatter role: 0 = auto        */
+    int32_t num_ctas;           /* persistent grid size: 0 = one CTA per SM             */
+    int64_t timeout_ns;         /* limit of every device-side wait: 0 = 2 s             */
+    int32_t debug_skip_publish; /* fault injection: 0 = off; m > 0 = never publish the
+                                   ready flag of m-tile m-1 (the consumer's bounded wait
+                                   then reports MOE_ERR_TIMEOUT)                         */
+    int32_t reserved;           /* must be 0                                            */
+} moe_shape_t;
+
+typedef struct moe_plan_info {
+    int32_t tile_m, tile_n, tile_k;   /* GEMM tile (rows, columns, reduction step)      */
+    int32_t stages;                   /* shared-memory pipeline depth                   */
+    int32_t num_ctas, producer_ctas;  /* persistent grid and its initial scatter role   */
+    int32_t sm_count;                 /* SMs of the plan's device                       */
+    int32_t smem_bytes;               /* dynamic shared memory of the fused kernel      */
+    int32_t max_mtiles;               /* upper bound on row tiles: floor(S/tile_m) + E  */
+    int32_t route_blocks;             /* CTAs of the routing kernel                     */
+    int64_t workspace_bytes;          /* size moe_plan reported                         */
+} moe_plan_info_t;
+
+/*
+ * moe_plan -- validate a shape and build a plan for `device`.
+ *   shape            in:  the layer shape and optional tuning fields.
+ *   device           in:  CUDA device ordinal the plan (and every later call)
+ *                         runs on; it must be current when calls are made.
+ *   plan             out: the new plan; release it with moe_plan_destroy.
+ *   workspace_bytes  out: size of the device workspace every moe_route and
+ *                         moe_dispatch_gemm call of this plan needs.  The
+ *                         caller allocates it, 256-byte aligned, and fills it
+ *                         with zeros ONCE before the first call (and again
+ *                         after any device error status); the calls return
+ *                         their counters to zero themselves.
+ * Host only (queries device attributes); launches nothing.
+ */
+MOE_API moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan,
+                      size_t* workspace_bytes);
+
+/* Release a plan (NULL is accepted). */
+MOE_API moe_status_t moe_plan_destroy(moe_plan_t plan);
+
+/* Copy the plan's chosen configuration into *info. */
+MOE_API moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info);
+
+/*
+ * moe_route -- the routing half of "MoE Dispatch + GEMM": choose each
+ * token's experts and lay out the destination rows.
+ *   logits   in:  fp32 [T][E] router logits (any bias already added); finite.
+ *   topk_idx out: int32 [T][k]; slot j holds the expert with the (j+1)-th
+ *                 largest logit; between equal logits the lower expert index
+ *                 comes first (-0.0 equals +0.0).
+ *   topk_w   out: fp32 [T][k]; softmax over all E logits of the token,
+ *                 evaluated at the chosen experts (not renormalised).
+ *   counts   out: int32 [E]; rows routed to each expert.
+ *   offsets  out: int32 [E+1]; exclusive prefix sum of counts, offsets[E] = S.
+ *   perm     out: int32 [S]; destination row -> source slot t*k+j.  Rows are
+ *                 grouped by expert (ascending), then by token, then slot.
+ *   dest     out: int32 [S]; the inverse of perm.
+ *   workspace in/out: the plan's workspace (see moe_plan).
+ * Launches two kernels on `stream`.  Results are identical bit for bit on
+ * every run (no atomics decide any order).
+ */
+MOE_API moe_status_t moe_route(moe_plan_t plan, const float* logits,
+                       int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets,
+                       int32_t* perm, int32_t* dest,
+                       void* workspace, void* stream);
+
+/*
+ * moe_dispatch_gemm -- the fused dispatch + per-expert grouped GEMM, one
+ * persistent kernel.  Scatter CTAs copy token rows into the rank receive
+ * buffers and publish a ready flag per 128-row tile; GEMM CTAs wait for each
+ * tile's flag and run it on the tensor cores (bf16 inputs, fp32
+ * accumulation) as soon as it is ready.
+ *   x        in:  bf16 [T][d] token rows.
+ *   offsets  in:  int32 [E+1] from moe_route (device).
+ *   perm     in:  int32 [S] from moe_route (device).
+ *   W        in:  bf16 [E][d][N] expert weights (N contiguous).
+ *   recv     in:  HOST array of R device pointers; recv[r] is rank r's receive
+ *                 buffer, bf16 [rank_capacity_rows][d].  Rank r owns experts
+ *                 [r*E/R, (r+1)*E/R); its buffer receives the destination rows
+ *                 [offsets[r*E/R], offsets[(r+1)*E/R]) in order (out).
+ *   Y        out: fp32 [S][N]; Y[i] = recv row of destination row i times
+ *                 W[e(i)], where e(i) is the expert whose segment holds i.
+ *                 Row order is the destination (expert-sorted) order; undoing
+ *                 the permutation is the caller's step.
+ *   workspace in/out: the plan's workspace.
+ *   dev_status in/out: device int32[4], zeroed by the caller before first use.
+ *                 The first device-side error writes {code, tile or row,
+ *                 expert, call epoch}; later errors do not overwrite it.
+ * Launches one kernel on `stream`.
+ */
+MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
+                               const int32_t* offsets, const int32_t* perm,
+                               const uint16_t* W, void* const* recv, float* Y,
+                               void* workspace, int32_t* dev_status, void* stream);
+
+/*
+ * moe_read_status -- synchronise `stream`, copy the 4-word device status to
+ * out[4] and return out[0] as a moe_status_t (MOE_ERR_CUDA if the copy or
+ * the synchronisation fails).  This is the one call that waits for the GPU.
+ */
+MOE_API moe_status_t moe_read_status(const int32_t* dev_status, void* stream, int32_t out[4]);
+
+/* Static string naming a status code. */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

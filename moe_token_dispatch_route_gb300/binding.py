@@ -1,0 +1,210 @@
+"""Thin ctypes binding of libmoe_gb300.so (the C ABI in include/moe.h).
+
+Argument marshalling only: tensors are handed over as raw device pointers
+together with the current CUDA stream; every step of the path runs in the
+library's kernels.  Importing this module does not need a GPU; the first
+call loads the library and raises if it has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+_lib = None
+
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CAPACITY", 7: "MOE_ERR_DEVICE",
+}
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_CAPACITY = 6
+MOE_ERR_DEVICE = 7
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        super().__init__(f"{call} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("k", ctypes.c_int32), ("N", ctypes.c_int32), ("num_ranks", ctypes.c_int32),
+        ("rank_capacity_rows", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+        ("producer_ctas", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("timeout_ns", ctypes.c_int64), ("debug_skip_publish", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
+        ("stages", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("producer_ctas", ctypes.c_int32),
+        ("sm_count", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("max_mtiles", ctypes.c_int32),
+        ("route_blocks", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
+            "moe_read_status", "moe_status_string")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmoe_gb300.so and declare its signatures (raises if it is missing)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first (__graft_entry__.build() or "
+            "python moe_token_dispatch_route_gb300/build.py); there is no fallback path")
+    lib = ctypes.CDLL(path)
+    P, I32, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_void_p
+    lib.moe_plan.argtypes = [P(Shape), ctypes.c_int, P(VP), P(ctypes.c_size_t)]
+    lib.moe_plan.restype = I32
+    lib.moe_plan_destroy.argtypes = [VP]
+    lib.moe_plan_destroy.restype = I32
+    lib.moe_plan_info.argtypes = [VP, P(PlanInfo)]
+    lib.moe_plan_info.restype = I32
+    lib.moe_route.argtypes = [VP] * 10
+    lib.moe_route.restype = I32
+    lib.moe_dispatch_gemm.argtypes = [VP] * 10
+    lib.moe_dispatch_gemm.restype = I32
+    lib.moe_read_status.argtypes = [VP, VP, P(I32)]
+    lib.moe_read_status.restype = I32
+    lib.moe_status_string.argtypes = [I32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, device=None) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, call: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, call)
+
+
+class Plan:
+    """Owns a moe_plan_t; `workspace_bytes` and `info` come from the library."""
+
+    def __init__(self, handle: int, workspace_bytes: int, shape: Shape, device: int):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+        self.shape = shape
+        self.device = device
+        info = PlanInfo()
+        _check(load_library().moe_plan_info(handle, ctypes.byref(info)), "moe_plan_info")
+        self.info = info.as_dict()
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            _lib.moe_plan_destroy(h)
+
+
+def moe_plan(T: int, d: int, E: int, k: int, N: int, num_ranks: int = 1,
+             rank_capacity_rows: int = 0, tile_n: int = 0, producer_ctas: int = 0,
+             num_ctas: int = 0, timeout_ns: int = 0, debug_skip_publish: int = 0,
+             device: int | None = None) -> Plan:
+    lib = load_library()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    shape = Shape(T, d, E, k, N, num_ranks, rank_capacity_rows, tile_n, producer_ctas, num_ctas,
+                  timeout_ns, debug_skip_publish, 0)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(lib.moe_plan(ctypes.byref(shape), dev, ctypes.byref(handle), ctypes.byref(ws)), "moe_plan")
+    return Plan(handle.value, ws.value, shape, dev)
+
+
+def moe_route(plan: Plan, logits, topk_idx, topk_w, counts, offsets, perm, dest, workspace,
+              stream=None) -> None:
+    rc = load_library().moe_route(plan.handle, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+                                  _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(dest),
+                                  _ptr(workspace), _stream(stream, plan.device))
+    _check(rc, "moe_route")
+
+
+def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, workspace, dev_status,
+                      stream=None) -> None:
+    arr = (ctypes.c_void_p * max(1, len(recv)))(*[_ptr(r) for r in recv])
+    rc = load_library().moe_dispatch_gemm(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm), _ptr(W),
+                                          ctypes.cast(arr, ctypes.c_void_p), _ptr(Y),
+                                          _ptr(workspace), _ptr(dev_status),
+                                          _stream(stream, plan.device))
+    _check(rc, "moe_dispatch_gemm")
+
+
+def moe_read_status(dev_status, stream=None) -> tuple[int, list[int]]:
+    out = (ctypes.c_int32 * 4)()
+    rc = load_library().moe_read_status(_ptr(dev_status), _stream(stream), out)
+    return rc, list(out)
+
+
+class MoeBuffers:
+    """Device buffers of one layer shape, allocated with PyTorch (the caller's
+    side of the ABI): routing outputs, R receive buffers, Y, workspace, status."""
+
+    def __init__(self, plan: Plan, device="cuda"):
+        s = plan.shape
+        S = s.T * s.k
+        R = s.num_ranks or 1
+        cap = s.rank_capacity_rows or S
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_idx = torch.empty(s.T, s.k, **i32)
+        self.topk_w = torch.empty(s.T, s.k, dtype=torch.float32, device=dev)
+        self.counts = torch.empty(s.E, **i32)
+        self.offsets = torch.empty(s.E + 1, **i32)
+        self.perm = torch.empty(S, **i32)
+        self.dest = torch.empty(S, **i32)
+        self.recv = [torch.empty(max(cap, 1), s.d, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        self.Y = torch.empty(S, s.N, dtype=torch.float32, device=dev)
+        self.workspace = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(4, **i32)
+
+
+def route(plan: Plan, logits, bufs: MoeBuffers, stream=None):
+    moe_route(plan, logits, bufs.topk_idx, bufs.topk_w, bufs.counts, bufs.offsets, bufs.perm,
+              bufs.dest, bufs.workspace, stream)
+
+
+def dispatch_gemm(plan: Plan, x, W, bufs: MoeBuffers, stream=None):
+    moe_dispatch_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.recv, bufs.Y, bufs.workspace,
+                      bufs.status, stream)
+
+
+def forward(plan: Plan, logits, x, W, bufs: MoeBuffers, stream=None):
+    """One pass of the whole path: routing, then the fused dispatch + grouped GEMM."""
+    route(plan, logits, bufs, stream)
+    dispatch_gemm(plan, x, W, bufs, stream)

@@ -1,0 +1,550 @@
+// Fused dispatch + per-expert grouped GEMM: one persistent kernel.
+//
+// The operation is the "MoE Dispatch + GEMM" row of the mKernel articles'
+// table of the five fused kernels: an all-to-all that routes token rows to
+// their expert ranks, and the per-expert grouped GEMM in the same kernel,
+// run on rows as soon as they land, without a staging round trip.  Their
+// design section describes persistent kernels whose CTAs assign themselves
+// roles, with a per-shape number of SMs per role.
+//
+// On one GB300 the all-to-all becomes a scatter into R per-rank receive
+// buffers in local HBM.  Design:
+//  * Grid = one CTA per SM (about 200 KB of shared memory each, so exactly one
+//    fits), 256 threads.  Each CTA takes a ticket from a workspace counter
+//    when it starts; the first `producer_ctas` tickets take the scatter role
+//    first.  Only CTAs that are running take tickets, so a GEMM CTA never
+//    waits for a scatter CTA that has not been scheduled.
+//  * Scatter role: all 8 warps copy destination rows (perm -> token row of x)
+//    into the rank buffers with 16-byte loads and stores, 4 rows per work
+//    unit, in the order the GEMM consumes them.  The last unit of each
+//    128-row tile publishes the tile's ready flag (release store of the call's
+//    epoch).  Then the CTA joins the GEMM role.
+//  * GEMM role, warp-specialised: warp 0 lane 0 claims tiles from a
+//    workspace counter (expert-major, then column tile, then row tile),
+//    waits for the row tile's flag (acquire, then a generic->async proxy
+//    fence) and streams A (receive rows, K-major) and B (W, N-major) through
+//    a multi-stage TMA ring with 128-byte swizzle; warp 1 lane 0 issues
+//    tcgen05.mma (M=128, N=tile_n, K=16; bf16 in, fp32 accumulation in
+//    TMEM, two accumulators so the epilogue of one tile overlaps the next
+//    tile's MMAs); warps 4-7 read the accumulator with tcgen05.ld and store
+//    the valid rows and columns of Y (fp32) with streaming stores.
+//  * Every wait is bounded (globaltimer).  A ready flag that never comes is
+//    reported as MOE_ERR_TIMEOUT and the tile is computed anyway, so the
+//    pipeline stays consistent; a pipeline wait that gives up reports
+//    MOE_ERR_DEVICE and all roles leave through the same teardown (drain of
+//    issued TMA loads and MMAs, TMEM release).  The last CTA to finish resets
+//    the workspace counters and records the epoch.
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kMaxStages = 8;
+constexpr int kEpiWarp0 = 4;  // warps 4..7: TMEM lane quarters 0..3
+
+struct TileInfo {
+    int e, m, n, mtile;
+    int row0;  // global destination row of the tile's first row
+    int rows;  // valid rows 1..128; -1 marks the end of the schedule
+    int rank;
+    int arow;  // first row inside the rank's receive buffer
+};
+
+struct SmemCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t sfull[kRing];
+    uint64_t sempty[kRing];
+    uint64_t mma_done;
+    TileInfo ring[kRing];
+    uint32_t tmem_base;
+    int abort;
+    int role;
+    uint32_t epoch;
+    int wsum[kThreads / 32];
+};
+
+struct Waiter {
+    volatile int* abort;
+    int32_t* status;
+    long long flag_timeout_ns;  // ready-flag waits
+    long long pipe_timeout_ns;  // pipeline mbarrier waits (generous: they may include a flag wait)
+    uint32_t epoch;
+};
+
+// Bounded mbarrier wait.  Returns false if the CTA is aborting or the wait
+// exceeded the timeout (then it reports MOE_ERR_DEVICE and starts the abort).
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Waiter& w, int where,
+                         bool honor_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 127u) == 0) {
+            if (honor_abort && *w.abort) return false;
+            if (global_timer_ns() - t0 > (uint64_t)w.pipe_timeout_ns) {
+                report_error(w.status, kStDevice, where, -1, (int)w.epoch);
+                *w.abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait for a row tile's ready flag.  On timeout the error is
+// reported and the caller proceeds (the tile's result is then undefined).
+__device__ void wait_flag(const uint32_t* flag, const Waiter& w, int mtile, int e) {
+    if (ld_acquire_gpu(flag) == w.epoch) return;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ld_acquire_gpu(flag) == w.epoch) return;
+        if ((i & 31u) == 0) {
+            if (*w.abort) return;
+            if (global_timer_ns() - t0 > (uint64_t)w.flag_timeout_ns) {
+                report_error(w.status, kStTimeout, mtile, e, (int)w.epoch);
+                return;
+            }
+        }
+    }
+}
+
+// Row tiles per expert -> exclusive prefix mt_base[0..E] (E <= 1024), all threads.
+__device__ void build_mtile_table(const int32_t* offsets, int E, int* mt_base, int* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int base = tid * 4;
+    int loc[4];
+    int sum = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = base + u;
+        int v = 0;
+        if (e < E) {
+            const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
+            v = (cnt + kTileM - 1) / kTileM;
+        }
+        loc[u] = v;
+        sum += v;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int pre = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) pre += wsum[w];
+        total += wsum[w];
+    }
+    int run = pre + incl - sum;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (base + u < E) mt_base[base + u] = run;
+        run += loc[u];
+    }
+    if (tid == 0) mt_base[E] = total;
+    __syncthreads();
+}
+
+// largest e in [0, E) with mt_base[e] <= u (u < mt_base[E])
+__device__ __forceinline__ int expert_of_mtile(const int* mt_base, int E, int u) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (mt_base[mid] <= u) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                         int nvec, int lane) {
+    int v = lane;
+    for (; v + 32 * 7 < nvec; v += 32 * 8) {
+        uint4 t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t[u] = __ldg(src + v + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[v + 32 * u] = t[u];
+    }
+    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
+}
+
+// Scatter role: 4-row work units in (row tile, unit) order over all scatter warps.
+__device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, int role,
+                             uint32_t epoch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = p.producer_ctas * (kThreads / 32);
+    const int gw = role * (kThreads / 32) + warp;
+    const int total_mtiles = mt_base[p.E];
+    const long long units = (long long)total_mtiles * kChunksPerTile;
+    const int e_per_rank = p.E / p.R;
+    const int nvec = p.d / 8;
+    for (long long c = gw; c < units; c += nwarps) {
+        const int mtile = (int)(c / kChunksPerTile);
+        const int sub = (int)(c % kChunksPerTile);
+        const int e = expert_of_mtile(mt_base, p.E, mtile);
+        const int m = mtile - mt_base[e];
+        const int seg0 = __ldg(p.offsets + e);
+        const int cnt = __ldg(p.offsets + e + 1) - seg0;
+        const int r_begin = m * kTileM + sub * kRowsPerChunk;
+        const int r_end = min(r_begin + kRowsPerChunk, cnt);
+        const int rank = e / e_per_rank;
+        const int rbase = __ldg(p.offsets + rank * e_per_rank);
+        for (int r = r_begin; r < r_end; ++r) {
+            const int row = seg0 + r;
+            const int local = row - rbase;
+            if (local >= p.cap) {
+                if (lane == 0) report_error(p.status, kStCapacity, row, rank, (int)epoch);
+                continue;
+            }
+            const int src = __ldg(p.perm + row) / p.k;
+            if (src < 0 || src >= p.T) {
+                if (lane == 0) report_error(p.status, kStDevice, -3, row, (int)epoch);
+                continue;
+            }
+            copy_row(reinterpret_cast<const uint4*>(p.x + (size_t)src * p.d),
+                     reinterpret_cast<uint4*>(p.recv[rank] + (size_t)local * p.d), nvec, lane);
+        }
+        // publish: every lane orders its stores, then one arrival per unit
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t prev = atomicAdd(p.chunk_cnt + mtile, 1u);
+            if (prev == (uint32_t)(kChunksPerTile - 1)) {
+                __threadfence();
+                p.chunk_cnt[mtile] = 0u;  // ready for the next call
+                fence_proxy_async_global();
+                if (mtile != p.skip_publish) st_release_gpu(p.flags + mtile, epoch);
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES>
+struct Cfg {
+    static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB
+    static constexpr int kBBytes = BN * kTileK * 2;      // BN/64 boxes of 64 x 64
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN);
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr size_t kSmem =
+        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + sizeof(int) * (kMaxE + 1);
+    static_assert(STAGES <= kMaxStages, "stages");
+    static_assert(BN == 128 || BN == 256, "tile_n");
+};
+
+template <int BN, int STAGES>
+__device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
+                         uint8_t* sA, uint8_t* sB, const Waiter& w) {
+    using C = Cfg<BN, STAGES>;
+    const uint32_t total_tiles = (uint32_t)mt_base[p.E] * (uint32_t)p.n_tiles;
+    const int e_per_rank = p.E / p.R;
+    tma_prefetch_map(&p.b_map);
+    for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int last_phase[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+    bool ok = true;
+    while (ok) {
+        if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) break;
+        const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
+        TileInfo ti;
+        if (tile >= total_tiles) {
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = 0;
+            ti.rows = -1;
+        } else {
+            const int u = (int)(tile / (uint32_t)p.n_tiles);
+            const int e = expert_of_mtile(mt_base, p.E, u);
+            const int mt_e = mt_base[e + 1] - mt_base[e];
+            const int local = (int)(tile - (uint32_t)mt_base[e] * (uint32_t)p.n_tiles);
+            ti.e = e;
+            ti.n = local / mt_e;
+            ti.m = local % mt_e;
+            ti.mtile = mt_base[e] + ti.m;
+            const int seg0 = __ldg(p.offsets + e);
+            const int cnt = __ldg(p.offsets + e + 1) - seg0;
+            ti.row0 = seg0 + ti.m * kTileM;
+            ti.rows = min(kTileM, cnt - ti.m * kTileM);
+            ti.rank = e / e_per_rank;
+            ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
+        }
+        ctl->ring[slot] = ti;
+        mbar_arrive(smem_addr(&ctl->sfull[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.rows < 0) break;
+
+        wait_flag(p.flags + ti.mtile, w, ti.mtile, ti.e);
+        fence_proxy_async_global();
+        const CUtensorMap* amap = &p.a_map[ti.rank];
+        const int brow = ti.e * p.d;
+        const int ncol = ti.n * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 2)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_addr(&ctl->full[stage]);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, ti.arow);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
+                            ncol + 64 * j, brow + kb * kTileK);
+            last_phase[stage] = (int)phase;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // no TMA write may still be landing in shared memory when the CTA exits
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s)
+        if (last_phase[s] >= 0) wait_bar(smem_addr(&ctl->full[s]), (uint32_t)last_phase[s], w, 3, false);
+}
+
+template <int BN, int STAGES>
+__device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, uint8_t* sB,
+                         uint32_t tmem_base, const Waiter& w) {
+    using C = Cfg<BN, STAGES>;
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    while (ok) {
+        if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 4)) break;
+        const int rows = ctl->ring[slot].rows;
+        mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (rows < 0) break;
+        if (!wait_bar(smem_addr(&ctl->tempty[acc]), aphase ^ 1u, w, 5)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 6)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+            const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
+                // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
+                //    1024 B apart (SBO); K step of 16 rows = +2048 B.
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(smem_addr(&ctl->empty[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit(smem_addr(&ctl->tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+    }
+    // every MMA issued by this thread completes before TMEM is released
+    umma_commit(smem_addr(&ctl->mma_done));
+    wait_bar(smem_addr(&ctl->mma_done), 0u, w, 7, false);
+}
+
+template <int BN, int STAGES>
+__device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
+                              const Waiter& w) {
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter of this warp
+    int slot = 0;
+    uint32_t sphase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (;;) {
+        const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 8);
+        if (!__all_sync(kFull, got)) break;
+        const TileInfo ti = ctl->ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.rows < 0) break;
+        const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 9);
+        if (!__all_sync(kFull, ready)) break;
+        tc_fence_after();
+        const int r = 32 * q + lane;
+        const bool valid = r < ti.rows;
+        float* yrow = p.Y + (size_t)(ti.row0 + (valid ? r : 0)) * p.N + (size_t)ti.n * BN;
+        const int ncols = min(BN, p.N - ti.n * BN);
+        const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(32 * q) << 16);
+        for (int c = 0; c < ncols; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32(tbase + (uint32_t)c, v);
+            tmem_ld_wait(v);
+            if (valid) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    if (c + i < ncols)
+                        __stcs(reinterpret_cast<float4*>(yrow + c + i),
+                               make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_addr(&ctl->tempty[acc]));
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+    }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    dispatch_gemm_kernel(const __grid_constant__ DispatchGemmParams p) {
+    using C = Cfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * C::kABytes;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sB + STAGES * C::kBBytes);
+    int* mt_base = reinterpret_cast<int*>(ctl + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&ctl->tfull[a]), 1);
+            mbar_init(smem_addr(&ctl->tempty[a]), 128);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(smem_addr(&ctl->sfull[r]), 1);
+            mbar_init(smem_addr(&ctl->sempty[r]), 1 + 4);  // MMA thread + 4 epilogue warps
+        }
+        mbar_init(smem_addr(&ctl->mma_done), 1);
+        ctl->abort = 0;
+        ctl->role = (int)atomicAdd(p.hdr + kHdrRoleCtr, 1u);
+        uint32_t ep = __ldcg(p.hdr + kHdrEpoch) + 1u;
+        ctl->epoch = ep == 0u ? 1u : ep;
+        mbar_fence_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    build_mtile_table(p.offsets, p.E, mt_base, ctl->wsum);  // contains __syncthreads
+    if (mt_base[p.E] > p.max_mtiles || __ldg(p.offsets + p.E) != p.T * p.k) {
+        // offsets that do not describe T*k rows: report, and schedule nothing
+        __syncthreads();
+        if (tid == 0) {
+            report_error(p.status, kStDevice, -2, __ldg(p.offsets + p.E), 0);
+            mt_base[p.E] = 0;
+            for (int e = 0; e < p.E; ++e) mt_base[e] = 0;
+        }
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint32_t epoch = ctl->epoch;
+    const int role = ctl->role;
+
+    if (role < p.producer_ctas) {
+        scatter_role(p, mt_base, role, epoch);
+        __syncthreads();
+    }
+
+    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
+    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
+    if (warp == 0) {
+        if (lane == 0) tma_role<BN, STAGES>(p, ctl, mt_base, sA, sB, w);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) mma_role<BN, STAGES>(p, ctl, sA, sB, tmem_base, w);
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        epilogue_role<BN, STAGES>(p, ctl, tmem_base, w);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.hdr + kHdrDoneCtr, 1u);
+        if (prev == gridDim.x - 1) {  // every CTA has finished with the counters
+            __threadfence();
+            p.hdr[kHdrTileCtr] = 0u;
+            p.hdr[kHdrRoleCtr] = 0u;
+            p.hdr[kHdrDoneCtr] = 0u;
+            p.hdr[kHdrEpoch] = epoch;
+            __threadfence();
+        }
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_cfg(const DispatchGemmParams& p, int grid, size_t smem, cudaStream_t stream) {
+    dispatch_gemm_kernel<BN, STAGES><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t dispatch_gemm_smem_bytes(int tile_n, int stages) {
+    if (tile_n == 256 && stages == 4) return Cfg<256, 4>::kSmem;
+    if (tile_n == 128 && stages == 6) return Cfg<128, 6>::kSmem;
+    return 0;
+}
+
+cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem) {
+    if (tile_n == 256 && stages == 4)
+        return cudaFuncSetAttribute(dispatch_gemm_kernel<256, 4>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (tile_n == 128 && stages == 6)
+        return cudaFuncSetAttribute(dispatch_gemm_kernel<128, 6>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages, size_t smem,
+                                 cudaStream_t stream) {
+    if (p.tile_n == 256 && stages == 4) return launch_cfg<256, 4>(p, grid, smem, stream);
+    if (p.tile_n == 128 && stages == 6) return launch_cfg<128, 6>(p, grid, smem, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

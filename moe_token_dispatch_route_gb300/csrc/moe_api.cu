@@ -1,0 +1,347 @@
+// C ABI of the library (declared in include/moe.h): argument validation,
+// the plan (tile configuration and role split), TMA tensor-map encoding and
+// the launches.  Host code only; the kernels live in route.cu and
+// dispatch_gemm.cu.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "moe.h"
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_plan_s {
+    moe_shape_t shape;
+    int device = 0;
+    int sm_count = 0;
+    int T = 0, d = 0, E = 0, k = 0, N = 0, R = 1, cap = 0;
+    long long S = 0;
+    int tile_n = 256, stages = 4, num_ctas = 0, producer_ctas = 0;
+    int max_mtiles = 0, route_blocks = 0;
+    size_t smem = 0;
+    WorkspaceLayout ws{};
+    long long timeout_ns = 0;
+    int skip_publish = -1;
+    // tensor maps, re-encoded only when the buffers change
+    std::mutex mu;
+    bool maps_valid = false;
+    const void* map_W = nullptr;
+    const void* map_recv[kMaxRanks] = {};
+    CUtensorMap a_maps[kMaxRanks];
+    CUtensorMap b_map;
+};
+
+namespace {
+
+constexpr long long kDefaultTimeoutNs = 2000000000LL;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Makes `dev` current for the duration of a call and restores the previous device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            prev = -1;
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 [rows][cols] row-major, 128-byte swizzle, box = box_cols x box_rows
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+moe_status_t validate_shape(const moe_shape_t& s) {
+    if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.N <= 0 || s.num_ranks < 0 ||
+        s.rank_capacity_rows < 0 || s.producer_ctas < 0 || s.num_ctas < 0 || s.timeout_ns < 0 ||
+        s.debug_skip_publish < 0 || s.reserved != 0)
+        return MOE_ERR_INVALID_ARG;
+    const int R = s.num_ranks == 0 ? 1 : s.num_ranks;
+    if (s.E > kMaxE || s.k > std::min(s.E, 32)) return MOE_ERR_UNSUPPORTED;
+    if (s.d % kTileK != 0 || s.d > 65536) return MOE_ERR_UNSUPPORTED;
+    if (s.N % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (R > kMaxRanks || s.E % R != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)s.T * s.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 256) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, size_t* workspace_bytes) {
+    if (!shape || !plan || !workspace_bytes || device < 0) return MOE_ERR_INVALID_ARG;
+    *plan = nullptr;
+    moe_status_t st = validate_shape(*shape);
+    if (st != MOE_OK) return st;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    DeviceGuard guard(device);
+    if (!guard.ok) return MOE_ERR_CUDA;
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+
+    moe_plan_s* p = new (std::nothrow) moe_plan_s();
+    if (!p) return MOE_ERR_INVALID_ARG;
+    p->shape = *shape;
+    p->device = device;
+    p->sm_count = sms;
+    p->T = shape->T;
+    p->d = shape->d;
+    p->E = shape->E;
+    p->k = shape->k;
+    p->N = shape->N;
+    p->R = shape->num_ranks == 0 ? 1 : shape->num_ranks;
+    p->S = (long long)p->T * p->k;
+    p->cap = shape->rank_capacity_rows == 0 ? (int)p->S : shape->rank_capacity_rows;
+    p->tile_n = shape->tile_n != 0 ? shape->tile_n : (p->N >= 256 ? 256 : 128);
+    p->stages = p->tile_n == 256 ? 4 : 6;
+    p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
+    if (p->smem == 0 || (int)p->smem > smem_optin) {
+        delete p;
+        return MOE_ERR_UNSUPPORTED;
+    }
+    p->num_ctas = shape->num_ctas != 0 ? std::min(shape->num_ctas, sms) : sms;
+    const double scatter_bytes = (double)p->S * p->d * 2.0;
+    int auto_p = (int)((scatter_bytes + (2 << 20) - 1) / (double)(2 << 20));
+    auto_p = std::max(8, std::min(auto_p, std::max(1, p->num_ctas / 4)));
+    p->producer_ctas = shape->producer_ctas != 0 ? shape->producer_ctas : auto_p;
+    p->producer_ctas = std::max(1, std::min(p->producer_ctas, p->num_ctas));
+    p->max_mtiles = (int)(p->S / kTileM) + p->E;
+    p->route_blocks = (p->T + kRouteChunk - 1) / kRouteChunk;
+    p->timeout_ns = shape->timeout_ns != 0 ? shape->timeout_ns : kDefaultTimeoutNs;
+    p->skip_publish = shape->debug_skip_publish > 0 ? shape->debug_skip_publish - 1 : -1;
+
+    size_t off = kHdrBytes;
+    p->ws.route_blk_off = off;
+    off = round_up(off + (size_t)std::max(1, p->route_blocks) * p->E * 4, 256);
+    p->ws.flags_off = off;
+    off = round_up(off + (size_t)p->max_mtiles * 4, 256);
+    p->ws.chunk_cnt_off = off;
+    off = round_up(off + (size_t)p->max_mtiles * 4, 256);
+    p->ws.total = off;
+
+    if (dispatch_gemm_prepare_attributes(p->tile_n, p->stages, p->smem) != cudaSuccess ||
+        route_prepare_attributes() != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return MOE_ERR_CUDA;
+    }
+    *plan = p;
+    *workspace_bytes = p->ws.total;
+    return MOE_OK;
+}
+
+moe_status_t moe_plan_destroy(moe_plan_t plan) {
+    delete plan;
+    return MOE_OK;
+}
+
+moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info) {
+    if (!plan || !info) return MOE_ERR_INVALID_ARG;
+    info->tile_m = kTileM;
+    info->tile_n = plan->tile_n;
+    info->tile_k = kTileK;
+    info->stages = plan->stages;
+    info->num_ctas = plan->num_ctas;
+    info->producer_ctas = plan->producer_ctas;
+    info->sm_count = plan->sm_count;
+    info->smem_bytes = (int32_t)plan->smem;
+    info->max_mtiles = plan->max_mtiles;
+    info->route_blocks = plan->route_blocks;
+    info->workspace_bytes = (int64_t)plan->ws.total;
+    return MOE_OK;
+}
+
+moe_status_t moe_route(moe_plan_t plan, const float* logits, int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* dest,
+                       void* workspace, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (plan->T > 0 && (!logits || !topk_idx || !topk_w || !perm || !dest ||
+                        !aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+                        !aligned(perm, 4) || !aligned(dest, 4)))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->T == 0) {
+        if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * plan->E, s) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (plan->E + 1), s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    RouteArgs a;
+    a.logits = logits;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.dest = dest;
+    a.hdr = reinterpret_cast<uint32_t*>(ws);
+    a.blk = reinterpret_cast<int32_t*>(ws + plan->ws.route_blk_off);
+    a.T = plan->T;
+    a.E = plan->E;
+    a.k = plan->k;
+    a.nb = plan->route_blocks;
+    if (launch_route(a, s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                               const int32_t* perm, const uint16_t* W, void* const* recv, float* Y,
+                               void* workspace, int32_t* dev_status, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
+    if (plan->T == 0) return MOE_OK;
+    if (!x || !offsets || !perm || !W || !recv || !Y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(offsets, 4) ||
+        !aligned(perm, 4))
+        return MOE_ERR_INVALID_ARG;
+    for (int r = 0; r < plan->R; ++r)
+        if (!recv[r] || !aligned(recv[r], 16)) return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return MOE_ERR_CUDA;
+
+    DispatchGemmParams prm;
+    {
+        std::lock_guard<std::mutex> lock(plan->mu);
+        bool same = plan->maps_valid && plan->map_W == W;
+        for (int r = 0; same && r < plan->R; ++r) same = plan->map_recv[r] == recv[r];
+        if (!same) {
+            plan->maps_valid = false;
+            for (int r = 0; r < plan->R; ++r)
+                if (!encode_bf16_2d(&plan->a_maps[r], recv[r], (uint64_t)plan->cap, (uint64_t)plan->d,
+                                    kTileK, kTileM))
+                    return MOE_ERR_CUDA;
+            if (!encode_bf16_2d(&plan->b_map, W, (uint64_t)plan->E * plan->d, (uint64_t)plan->N, 64,
+                                kTileK))
+                return MOE_ERR_CUDA;
+            plan->map_W = W;
+            for (int r = 0; r < plan->R; ++r) plan->map_recv[r] = recv[r];
+            plan->maps_valid = true;
+        }
+        std::memset(&prm, 0, sizeof prm);
+        for (int r = 0; r < plan->R; ++r) prm.a_map[r] = plan->a_maps[r];
+        prm.b_map = plan->b_map;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    prm.x = x;
+    prm.offsets = offsets;
+    prm.perm = perm;
+    for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
+    prm.Y = Y;
+    prm.hdr = reinterpret_cast<uint32_t*>(ws);
+    prm.flags = reinterpret_cast<uint32_t*>(ws + plan->ws.flags_off);
+    prm.chunk_cnt = reinterpret_cast<uint32_t*>(ws + plan->ws.chunk_cnt_off);
+    prm.status = dev_status;
+    prm.timeout_ns = plan->timeout_ns;
+    prm.T = plan->T;
+    prm.d = plan->d;
+    prm.E = plan->E;
+    prm.k = plan->k;
+    prm.N = plan->N;
+    prm.R = plan->R;
+    prm.cap = plan->cap;
+    prm.tile_n = plan->tile_n;
+    prm.n_tiles = (plan->N + plan->tile_n - 1) / plan->tile_n;
+    prm.k_blocks = plan->d / kTileK;
+    prm.producer_ctas = plan->producer_ctas;
+    prm.max_mtiles = plan->max_mtiles;
+    prm.skip_publish = plan->skip_publish;
+    if (launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_read_status(const int32_t* dev_status, void* stream, int32_t out[4]) {
+    if (!dev_status || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpyAsync(out, dev_status, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return static_cast<moe_status_t>(out[0]);
+}
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+// Internal declarations shared by the library's translation units: the
+// workspace layout, the launch parameter blocks and the sm_103a inline-PTX
+// helpers (mbarrier, TMA, tcgen05/TMEM, proxy fences).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- constants
+
+constexpr int kRouteChunk = 64;     // tokens per routing CTA
+constexpr int kRouteThreads = 256;  // 8 warps
+
+constexpr int kTileM = 128;         // GEMM rows per tile (one UMMA M=128)
+constexpr int kTileK = 64;          // bf16 elements per 128-byte swizzle row
+constexpr int kUmmaK = 16;          // K of one tcgen05.mma kind::f16
+constexpr int kRowsPerChunk = 4;    // destination rows per scatter work unit
+constexpr int kChunksPerTile = kTileM / kRowsPerChunk;
+constexpr int kThreads = 256;       // fused kernel: 8 warps
+constexpr int kRing = 8;            // tile-schedule ring entries
+constexpr int kMaxRanks = 32;
+constexpr int kMaxE = 1024;
+
+// device status codes (same numbers as moe_status_t)
+constexpr int kStTimeout = 5;
+constexpr int kStCapacity = 6;
+constexpr int kStDevice = 7;
+
+// workspace header words (u32)
+constexpr int kHdrEpoch = 0;
+constexpr int kHdrTileCtr = 8;      // separate 32-byte sectors
+constexpr int kHdrRoleCtr = 16;
+constexpr int kHdrDoneCtr = 24;
+constexpr int kHdrRouteTicket = 32;
+constexpr size_t kHdrBytes = 256;
+
+struct WorkspaceLayout {
+    size_t route_blk_off;   // int32 [route_blocks][E]
+    size_t flags_off;       // u32 [max_mtiles]
+    size_t chunk_cnt_off;   // u32 [max_mtiles]
+    size_t total;
+};
+
+// ---------------------------------------------------------------- launches
+
+struct RouteArgs {
+    const float* logits;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* dest;
+    uint32_t* hdr;
+    int32_t* blk;     // [nb][E] per-CTA counts, then per-CTA bases
+    int T, E, k, nb;
+};
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+cudaError_t route_prepare_attributes();
+
+struct DispatchGemmParams {
+    CUtensorMap a_map[kMaxRanks];   // rank receive buffers, bf16 [cap][d], box 64 x 128
+    CUtensorMap b_map;              // W viewed as bf16 [E*d][N], box 64 x 64
+    const uint16_t* x;
+    const int32_t* offsets;
+    const int32_t* perm;
+    uint16_t* recv[kMaxRanks];
+    float* Y;
+    uint32_t* hdr;
+    uint32_t* flags;
+    uint32_t* chunk_cnt;
+    int32_t* status;
+    long long timeout_ns;
+    int T, d, E, k, N, R, cap;
+    int tile_n, n_tiles, k_blocks;
+    int producer_ctas;
+    int max_mtiles;                 // size of flags[] and chunk_cnt[]
+    int skip_publish;               // m-tile whose flag is never published, or -1
+};
+
+cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
+                                 size_t smem, cudaStream_t stream);
+size_t dispatch_gemm_smem_bytes(int tile_n, int stages);
+cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem);
+
+// ---------------------------------------------------------------- PTX helpers
+
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// first error wins; later ones are dropped
+__device__ __forceinline__ void report_error(int32_t* status, int code, int a0, int a1, int a2) {
+    if (atomicCAS(status, 0, code) == 0) {
+        status[1] = a0;
+        status[2] = a1;
+        status[3] = a2;
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// ---- TMA (tensor, tiled, global -> shared, completes on an mbarrier)
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// ---- tcgen05 / TMEM
+
+__device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(holder_smem), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]; bf16 inputs, fp32 accumulator, one thread issues
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// the mbarrier gets one arrival once every earlier tcgen05 op of this thread is done
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane (base + i)
+__device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// waits for this thread's tcgen05.ld; the registers are tied in so no use moves above it
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of tcgen05.mma, 128-byte swizzle:
+// bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
+// 32-45 stride byte offset >> 4, 46-48 = 0b001, 49-51 base offset (0: the
+// swizzle atoms are 1024-byte aligned), 61-63 layout (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+#endif  // __CUDACC__
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B MN-major
+// (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t idesc_bf16_f32_kmajA_mnmajB(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+}  // namespace moe

@@ -1,0 +1,116 @@
+"""Helpers of the GPU parity tests: run the CUDA path through the C ABI and
+compare it with the CPU oracle.
+
+Parity bar: routing indices, counts, offsets, permutation, inverse and the
+receive buffers bit for bit; gate weights within 1e-5 absolute (fp32 expf
+against fp64 exp); Y within max|err| <= 1e-2 * RMS(ref) and
+||err||_F <= 5e-3 * ||ref||_F against the oracle's fp64 sums.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from moe_token_dispatch_route_gb300 import binding, workloads
+
+TOL_MAX_REL_RMS = 1e-2
+TOL_FRO = 5e-3
+TOL_GATE = 1e-5
+
+
+def run_path(wl, inp, device="cuda", poison=True, **plan_kw):
+    """Plan, allocate, poison outputs with NaN, run route + dispatch_gemm."""
+    dev = torch.device(device)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **plan_kw)
+    bufs = binding.MoeBuffers(plan, dev)
+    if poison:
+        bufs.Y.fill_(float("nan"))
+        for r in bufs.recv:
+            r.fill_(float("nan"))
+    x = inp["x"].to(dev)
+    W = inp["W"] if inp["W"].device == dev else inp["W"].to(dev)
+    logits = inp["logits"].to(dev)
+    binding.forward(plan, logits, x, W, bufs)
+    rc, status = binding.moe_read_status(bufs.status)
+    return plan, bufs, rc, status
+
+
+def check_route(bufs, ref, k):
+    for key in ("topk_idx", "counts", "offsets", "perm", "dest"):
+        got = getattr(bufs, key).cpu().numpy().reshape(ref[key].shape)
+        assert np.array_equal(got, ref[key]), f"{key} differs from the oracle"
+    w = bufs.topk_w.cpu().double().numpy()
+    assert np.max(np.abs(w - ref["topk_w"])) <= TOL_GATE
+
+
+def rank_rows(ref, E, R):
+    return oracle.rank_base(ref["offsets"], R)
+
+
+def check_recv(bufs, x_bits, ref, k, R, rows=None):
+    """Each rank buffer's defined rows equal the oracle's gathered rows, bit for bit.
+    `rows`: optional precomputed oracle gather (global destination order)."""
+    E = ref["offsets"].shape[0] - 1
+    base = rank_rows(ref, E, R)
+    if rows is None:
+        rows = oracle.gather(x_bits, ref["perm"], k)
+    for r in range(R):
+        n = int(base[r + 1] - base[r])
+        got = bufs.recv[r][:n].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, rows[base[r]:base[r + 1]]), f"rank {r} receive rows differ"
+
+
+def check_Y(Y: np.ndarray, Yref: np.ndarray):
+    assert Y.shape == Yref.shape
+    assert np.isfinite(Y).all(), "unwritten (NaN) or non-finite output"
+    err = np.abs(Y - Yref)
+    rms = float(np.sqrt(np.mean(Yref ** 2)))
+    assert float(err.max()) <= TOL_MAX_REL_RMS * rms, (float(err.max()), rms)
+    assert float(np.linalg.norm(Y - Yref)) <= TOL_FRO * float(np.linalg.norm(Yref))
+    return float(err.max()), rms
+
+
+def sample_rows_cols(ref, N, tile_m=128, tile_n=256, n_random=48, seed=0):
+    """Rows at every expert's first/last row and tile boundaries, plus random
+    rows; columns at the edges, tile boundaries and random."""
+    rng = np.random.default_rng(seed)
+    off = ref["offsets"]
+    S = int(off[-1])
+    rows = set()
+    for e in range(len(off) - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            rows.update({a, b - 1})
+            for t in range(a + tile_m - 1, b, tile_m):
+                rows.update({t, min(t + 1, b - 1)})
+    rows = sorted(rows)
+    if len(rows) > 96:
+        rows = sorted(rng.choice(rows, 96, replace=False).tolist())
+    rows = sorted(set(rows) | set(rng.integers(0, S, n_random).tolist()))
+    cols = {0, N - 1, min(N - 1, tile_n - 1), min(N - 1, tile_n), N // 2}
+    cols |= set(rng.integers(0, N, 12).tolist())
+    return rows, sorted(cols)
+
+
+def check_Y_sampled(Y_dev: torch.Tensor, x_bits, W_dev: torch.Tensor, ref, k, rows, cols):
+    """Oracle entries one by one at the sampled (row, col) grid."""
+    assert not torch.isnan(Y_dev).any().item(), "unwritten (NaN) output rows"
+    perm_sub = ref["perm"][rows]
+    a_rows = oracle.gather(x_bits, perm_sub, k)
+    cols_t = torch.tensor(cols, device=W_dev.device)
+    got = Y_dev[torch.tensor(rows, device=Y_dev.device)][:, cols_t].cpu().double().numpy()
+    want = np.empty_like(got)
+    cache = {}
+    for i, row in enumerate(rows):
+        e = oracle.expert_of_row(ref["offsets"], row)
+        if e not in cache:
+            cache[e] = workloads.bf16_bits(W_dev[e][:, cols_t])
+        Wc = cache[e]
+        for j in range(len(cols)):
+            want[i, j] = oracle.gemm_entry(a_rows[i], Wc, j)
+    err = np.abs(got - want)
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    assert float(err.max()) <= TOL_MAX_REL_RMS * rms, (float(err.max()), rms)
+    assert float(np.linalg.norm(got - want)) <= TOL_FRO * float(np.linalg.norm(want))
+    return float(err.max()), rms
