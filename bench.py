@@ -1,0 +1,350 @@
+#!/usr/bin/env python3
+"""Benchmark of the whole hot path: routing + fused dispatch/grouped GEMM.
+
+One step = moe_route (top-k, histogram, prefix sum, permutation) followed by
+moe_dispatch_gemm (scatter into the rank receive buffers + per-expert GEMM)
+over one batch of synthetic inputs already resident in HBM.  The default
+workload is the Mixtral-shaped layer (T=8192, d=4096, E=8, top-2, N=14336).
+
+Prints one JSON line (rank 0).  `value` is TFLOP/s of the whole step
+(2*T*k*d*N FLOPs / step time); `e2e` is the same metric through the same C
+ABI with the step's inputs copied from pinned host memory and Y copied back
+inside the timed region.  `--impl reference` times the CPU oracle instead.
+
+Multi-GPU (torchrun, one rank per GPU): the path has no multi-GPU exchange
+in this library, so every rank runs an independent replica (weak scaling);
+the timed region is bracketed by barriers and the max over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused dispatch+grouped-GEMM TFLOP/s and tokens/s at 1 GB300; % of bf16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SRC = os.path.join(ROOT, "moe_token_dispatch_route_gb300", "csrc", "dispatch_gemm.cu")
+
+
+def _args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--producer-ctas", type=int, default=0)
+    return ap.parse_args(argv)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _traffic_per_launch(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when absent or when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"dispatch_gemm_{workload}_traffic.txt")
+    try:
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    vals[key.strip()] = val.strip()
+        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        if vals.get("kernel_source_sha256_16") != src_hash:
+            return None
+        return float(vals["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float across the process group (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(wl, target_s: float = 12.0, rows=None):
+    """The CPU oracle, as it stands, on a bounded sample of the workload:
+    routing of all T tokens, then gather + fp64 grouped GEMM of the first
+    `rows` destination rows.  Returns (TFLOP/s on the sampled GEMM work, info)."""
+    import numpy as np
+
+    import oracle
+    from moe_token_dispatch_route_gb300 import workloads
+
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    L = inp["logits"].numpy()
+    xb = workloads.bf16_bits(inp["x"])
+    if rows is None:
+        rows = 128
+    t0 = time.perf_counter()
+    ref = oracle.route(L, wl.k)
+    t_route = time.perf_counter() - t0
+    e0 = int(np.searchsorted(ref["offsets"], 0, side="right") - 1)
+    sub = ref["perm"][:rows]
+    # experts covering the first `rows` destination rows
+    experts = sorted({oracle.expert_of_row(ref["offsets"], r) for r in range(rows)})
+    Ws = workloads.make_weights(workloads.custom("w", wl.T, wl.d, max(experts) + 1, 1, wl.N), seed=0)
+    Wb = workloads.bf16_bits(Ws)
+    off = np.minimum(ref["offsets"][: max(experts) + 2], rows).astype(np.int32)
+    t1 = time.perf_counter()
+    a_rows = oracle.gather(xb, sub, wl.k)
+    oracle.grouped_gemm(a_rows, Wb, off)
+    t_gemm = time.perf_counter() - t1
+    flops = 2.0 * rows * wl.d * wl.N
+    info = {"sample": f"routing of all {wl.T} tokens ({t_route:.2f} s) + gather and fp64 GEMM of the "
+                      f"first {rows} destination rows ({t_gemm:.2f} s); TFLOP/s over the sampled GEMM "
+                      f"FLOPs and the whole sample time", "cores": 1, "kind": "oracle"}
+    del e0
+    return flops / (t_route + t_gemm) / 1e12, info, t_route + t_gemm
+
+
+def run_reference(args, wl):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    # each step: routing of all tokens + GEMM of a row sample sized so the run stays short
+    per_step_budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    rows = 8
+    val, info, secs = cpu_baseline(wl, rows=rows)
+    scale = max(1, min(512, int(rows * per_step_budget / max(secs, 1e-3))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        v, info, secs = cpu_baseline(wl, rows=scale)
+        if i >= args.warmup:
+            times.append((v, secs))
+    value = statistics.median(v for v, _ in times)
+    ms = 1000.0 * statistics.median(s for _, s in times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**wl.describe(), "sample_rows_per_step": scale},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import torch
+
+    from moe_token_dispatch_route_gb300 import binding, workloads
+
+    world, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from moe_token_dispatch_route_gb300 import build as _build
+    _build.build()
+
+    inp = workloads.make_inputs(wl, seed=0, w_device=dev)
+    x = inp["x"].to(dev)
+    W = inp["W"]
+    logits = inp["logits"].to(dev)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n,
+                            producer_ctas=args.producer_ctas, device=local)
+    bufs = binding.MoeBuffers(plan, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        binding.forward(plan, logits, x, W, bufs, stream)
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"device status after warm-up: {st}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.fill_(float(i))  # evict L2 between steps (outside the events)
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            binding.route(plan, logits, bufs, stream)
+            e1.record(stream)
+            binding.dispatch_gemm(plan, x, W, bufs, stream)
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"device status after timed steps: {st}")
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    route_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dg_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_s = sum(step_ms) / 1000.0
+    total_s = max_over_ranks(total_s, world, dev)
+
+    # end to end through the same ABI: pinned host inputs in, Y out, every step
+    x_h = inp["x"].pin_memory()
+    l_h = inp["logits"].pin_memory()
+    y_h = torch.empty(bufs.Y.shape, dtype=bufs.Y.dtype).pin_memory()
+    x_d = torch.empty_like(x)
+    l_d = torch.empty_like(logits)
+    E2E = max(3, args.e2e_steps)
+    for _ in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        binding.forward(plan, l_d, x_d, W, bufs, stream)
+        y_h.copy_(bufs.Y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E2E)]
+    for i in range(E2E):
+        flush.fill_(float(i))
+        a, b = eev[i]
+        a.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        binding.forward(plan, l_d, x_d, W, bufs, stream)
+        y_h.copy_(bufs.Y, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / 1000.0, world, dev)
+    h2d = x_h.numel() * x_h.element_size() + l_h.numel() * l_h.element_size()
+    d2h = y_h.numel() * y_h.element_size()
+
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    hbm_peak, tf_peak, peak_src = _peaks()
+    flops = wl.flops
+    value = world * K * flops / total_s / 1e12
+    dg_avg_s = statistics.mean(dg_ms) / 1000.0
+    achieved = flops / dg_avg_s / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**wl.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "tile_n": plan.info["tile_n"], "producer_ctas": plan.info["producer_ctas"],
+                   "num_ctas": plan.info["num_ctas"], "stages": plan.info["stages"]},
+        "tokens_per_s": world * K * wl.T / total_s,
+        "pct_bf16_peak": 100.0 * value / world / tf_peak,
+        "route_ms": statistics.median(route_ms),
+        "dispatch_gemm_ms": statistics.median(dg_ms),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf_peak, "traffic": _traffic_per_launch(wl.name),
+                     "peak_source": f"{peak_src} (bf16 burst)", "kernel": "dispatch_gemm_kernel"},
+        "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        v, info, _ = cpu_baseline(wl)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, **info}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = _args(argv)
+    from moe_token_dispatch_route_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
