@@ -183,6 +183,35 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
  */
 MOE_API moe_status_t moe_read_status(const int32_t* dev_status, void* stream, int32_t out[4]);
 
+/*
+ * moe_route_noalloc -- moe_route for callers that cannot allocate device
+ * memory.  The pages describe no such variant; it exists for embedders that
+ * are not allowed to call cudaMalloc themselves: for example a plugin inside
+ * an inference server or framework that owns every byte of device memory and
+ * forbids allocation after start-up, or a code path that must not fail on an
+ * out-of-memory error.  It computes exactly what moe_route computes (same
+ * kernels, same outputs, bit for bit) but takes no workspace: its scratch (a
+ * per-CTA count table and a ticket counter) lives in a static device array
+ * of 1 MiB + 256 bytes inside the library, which every GPU that loads the
+ * library holds until the process exits.  Arguments as for moe_route.
+ *  - Limit: ceil(T/64) * E <= 262144 (for example T = 16384 with E <= 1024,
+ *    or T = 65536 with E <= 256).  A larger plan returns MOE_ERR_UNSUPPORTED
+ *    before any launch.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    routine.  It clears the ticket counter with cudaMemsetAsync on `stream`
+ *    before its launch; the count table is fully rewritten by every call.
+ *  - Every call shares the one array, which keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams, or different host
+ *    threads without ordering) race and give wrong results.
+ */
+MOE_API moe_status_t moe_route_noalloc(moe_plan_t plan, const float* logits,
+                                       int32_t* topk_idx, float* topk_w,
+                                       int32_t* counts, int32_t* offsets,
+                                       int32_t* perm, int32_t* dest, void* stream);
+
 /* Static string naming a status code. */
 MOE_API const char* moe_status_string(moe_status_t status);
 

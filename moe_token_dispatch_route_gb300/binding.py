@@ -61,7 +61,7 @@ class PlanInfo(ctypes.Structure):
 
 
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
-            "moe_read_status", "moe_status_string")
+            "moe_read_status", "moe_status_string", "moe_route_noalloc")
 
 
 def load_library(path: str = LIB_PATH):
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
+    lib.moe_route_noalloc.argtypes = [VP] * 9
+    lib.moe_route_noalloc.restype = I32
     lib.moe_status_string.argtypes = [I32]
     lib.moe_status_string.restype = ctypes.c_char_p
     if path == LIB_PATH:
@@ -153,6 +155,16 @@ def moe_route(plan: Plan, logits, topk_idx, topk_w, counts, offsets, perm, dest,
                                   _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(dest),
                                   _ptr(workspace), _stream(stream, plan.device))
     _check(rc, "moe_route")
+
+
+def moe_route_noalloc(plan: Plan, logits, topk_idx, topk_w, counts, offsets, perm, dest,
+                      stream=None) -> None:
+    """moe_route without a workspace: the library's static device scratch is used
+    instead (for callers that cannot allocate device memory)."""
+    rc = load_library().moe_route_noalloc(plan.handle, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+                                          _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(dest),
+                                          _stream(stream, plan.device))
+    _check(rc, "moe_route_noalloc")
 
 
 def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, workspace, dev_status,

@@ -108,6 +108,19 @@ moe_status_t validate_shape(const moe_shape_t& s) {
 
 }  // namespace
 
+namespace moe {
+// Shape fields the routing launch needs, for entry points defined in other files.
+bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks, int* device) {
+    if (!plan) return false;
+    *T = plan->T;
+    *E = plan->E;
+    *k = plan->k;
+    *route_blocks = plan->route_blocks;
+    *device = plan->device;
+    return true;
+}
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_status_string(moe_status_t s) {

@@ -1,0 +1,61 @@
+"""moe_route_noalloc: the routing entry point for callers that are not
+allowed to allocate device memory (for example a plugin in a host framework
+that owns all device memory).  It keeps its scratch in a static device array
+inside the library instead of a caller workspace.
+
+Checked through the C ABI against moe_route (the workspace entry point) on
+the same inputs, for two calls in a row with different inputs, so that
+leftovers of the first call in the shared array cannot go unnoticed.  This
+file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_token_dispatch_route_gb300 import binding, workloads
+from tests.gpu_util import TOL_GATE
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("topk_idx", "counts", "offsets", "perm", "dest")
+
+
+def _outputs(plan, dev):
+    s = plan.shape
+    S = s.T * s.k
+    i32 = dict(dtype=torch.int32, device=dev)
+    return {"topk_idx": torch.full((s.T, s.k), -1, **i32),
+            "topk_w": torch.full((s.T, s.k), float("nan"), dtype=torch.float32, device=dev),
+            "counts": torch.full((s.E,), -1, **i32), "offsets": torch.full((s.E + 1,), -1, **i32),
+            "perm": torch.full((S,), -1, **i32), "dest": torch.full((S,), -1, **i32)}
+
+
+def _args(o):
+    return (o["topk_idx"], o["topk_w"], o["counts"], o["offsets"], o["perm"], o["dest"])
+
+
+@pytest.mark.parametrize("name", ["finegrained", "deepseek_v3"])
+def test_noalloc_route_matches_workspace_route_twice(name):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = workloads.WORKLOADS[name]
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R)
+    ws = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
+    for call, seed in enumerate((11, 12)):
+        logits = workloads.make_inputs(wl, seed=seed, with_weights=False)["logits"].to(dev)
+        want = _outputs(plan, dev)
+        binding.moe_route(plan, logits, *_args(want), ws)
+        got = _outputs(plan, dev)
+        binding.moe_route_noalloc(plan, logits, *_args(got))
+        torch.cuda.synchronize()
+        for key in KEYS:
+            assert torch.equal(got[key], want[key]), f"call {call}: {key}"
+        err = (got["topk_w"].double() - want["topk_w"].double()).abs().max().item()
+        assert err <= TOL_GATE, f"call {call}: gate weights differ by {err}"
+
+
+def test_noalloc_route_rejects_plans_beyond_its_scratch():
+    # ceil(T/64) * E = 1025 * 256 > 262144: refused before any launch
+    plan = binding.moe_plan(64 * 1025, 64, 256, 8, 16)
+    with pytest.raises(binding.MoeError) as exc:
+        binding.moe_route_noalloc(plan, None, None, None, None, None, None, None)
+    assert exc.value.status == binding.MOE_ERR_UNSUPPORTED
