@@ -480,8 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int role = ctl->role;
 
     if (role < p.producer_ctas) {
+        unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
+        if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
         scatter_role(p, mt_base, role, epoch);
         __syncthreads();
+        if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }
 
     const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
@@ -511,6 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.hdr[kHdrRoleCtr] = 0u;
             p.hdr[kHdrDoneCtr] = 0u;
             p.hdr[kHdrEpoch] = epoch;
+            // scatter window of this call, for measurement; accumulators back to zero
+            unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
+            const unsigned long long inv = atomicExch(w64 + kHdrScatterInvStart / 2, 0ull);
+            const unsigned long long end = atomicExch(w64 + kHdrScatterEnd / 2, 0ull);
+            w64[kHdrLastScatterStart / 2] = ~inv;
+            w64[kHdrLastScatterEnd / 2] = end;
             __threadfence();
         }
     }

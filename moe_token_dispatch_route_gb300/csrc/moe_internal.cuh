@@ -35,6 +35,10 @@ constexpr int kHdrTileCtr = 8;      // separate 32-byte sectors
 constexpr int kHdrRoleCtr = 16;
 constexpr int kHdrDoneCtr = 24;
 constexpr int kHdrRouteTicket = 32;
+constexpr int kHdrScatterInvStart = 40;  // u64: max of ~globaltimer at scatter start (this call)
+constexpr int kHdrScatterEnd = 42;       // u64: max of globaltimer at scatter end (this call)
+constexpr int kHdrLastScatterStart = 48; // u64: scatter window of the last finished call, ns
+constexpr int kHdrLastScatterEnd = 50;   // u64
 constexpr size_t kHdrBytes = 256;
 
 struct WorkspaceLayout {
