@@ -113,8 +113,8 @@ __device__ void wait_flag(const uint32_t* flag, const Waiter& w, int mtile, int 
     }
 }
 
-// Row tiles per expert -> exclusive prefix mt_base[0..E] (E <= 1024), all threads.
-__device__ void build_mtile_table(const int32_t* offsets, int E, int* mt_base, int* wsum) {
+// Per-expert ceil(count / div) -> exclusive prefix table[0..E] (E <= 1024), all threads.
+__device__ void build_expert_table(const int32_t* offsets, int E, int div, int* table, int* wsum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int base = tid * 4;
     int loc[4];
@@ -125,7 +125,7 @@ __device__ void build_mtile_table(const int32_t* offsets, int E, int* mt_base, i
         int v = 0;
         if (e < E) {
             const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
-            v = (cnt + kTileM - 1) / kTileM;
+            v = (cnt + div - 1) / div;
         }
         loc[u] = v;
         sum += v;
@@ -146,80 +146,100 @@ __device__ void build_mtile_table(const int32_t* offsets, int E, int* mt_base, i
     int run = pre + incl - sum;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        if (base + u < E) mt_base[base + u] = run;
+        if (base + u < E) table[base + u] = run;
         run += loc[u];
     }
-    if (tid == 0) mt_base[E] = total;
+    if (tid == 0) table[E] = total;
     __syncthreads();
 }
 
-// largest e in [0, E) with mt_base[e] <= u (u < mt_base[E])
-__device__ __forceinline__ int expert_of_mtile(const int* mt_base, int E, int u) {
+// largest e in [0, E) with table[e] <= u (u < table[E]); empty experts are skipped
+__device__ __forceinline__ int expert_of(const int* table, int E, int u) {
     int lo = 0, hi = E;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (mt_base[mid] <= u) lo = mid;
+        if (table[mid] <= u) lo = mid;
         else hi = mid;
     }
     return lo;
 }
 
-__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                         int nvec, int lane) {
-    int v = lane;
-    for (; v + 32 * 7 < nvec; v += 32 * 8) {
-        uint4 t[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t[u] = __ldg(src + v + 32 * u);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) dst[v + 32 * u] = t[u];
-    }
-    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
-}
+// Scatter role: all 8 warps of a scatter CTA copy token rows into the rank
+// receive buffers with 16-byte loads and stores.
+//
+// Work unit = up to 4 consecutive destination rows of one expert inside one
+// 128-row tile; only non-empty units exist (unit_base holds the per-expert
+// prefix of ceil(count/4)).  Units are visited in destination order, strided
+// over all scatter warps of all scatter CTAs, so the earliest tiles fill
+// first.  Each lane keeps 16 independent 16-byte loads in flight (4 rows x 4
+// vectors).  After a unit, lane 0 fences (cumulative over the warp's stores
+// through __syncwarp) and counts the unit in; the last unit of a tile
+// releases the tile's ready flag with the call's epoch.
+constexpr int kScatterVec = 4;
 
-// Scatter role: 4-row work units in (row tile, unit) order over all scatter warps.
-__device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, int role,
-                             uint32_t epoch) {
+__device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
+                             int role, uint32_t epoch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = p.producer_ctas * (kThreads / 32);
     const int gw = role * (kThreads / 32) + warp;
-    const int total_mtiles = mt_base[p.E];
-    const long long units = (long long)total_mtiles * kChunksPerTile;
+    const int total_units = unit_base[p.E];
     const int e_per_rank = p.E / p.R;
     const int nvec = p.d / 8;
-    for (long long c = gw; c < units; c += nwarps) {
-        const int mtile = (int)(c / kChunksPerTile);
-        const int sub = (int)(c % kChunksPerTile);
-        const int e = expert_of_mtile(mt_base, p.E, mtile);
-        const int m = mtile - mt_base[e];
+    for (int c = gw; c < total_units; c += nwarps) {
+        const int e = expert_of(unit_base, p.E, c);
+        const int j = c - unit_base[e];  // unit inside the expert
         const int seg0 = __ldg(p.offsets + e);
         const int cnt = __ldg(p.offsets + e + 1) - seg0;
-        const int r_begin = m * kTileM + sub * kRowsPerChunk;
-        const int r_end = min(r_begin + kRowsPerChunk, cnt);
+        const int r_begin = j * kRowsPerChunk;
+        const int nrows = min(kRowsPerChunk, cnt - r_begin);
         const int rank = e / e_per_rank;
         const int rbase = __ldg(p.offsets + rank * e_per_rank);
-        for (int r = r_begin; r < r_end; ++r) {
-            const int row = seg0 + r;
-            const int local = row - rbase;
+        // lane r < nrows looks up row r of the unit
+        int tok = -1, local = -1;
+        if (lane < nrows) {
+            const int row = seg0 + r_begin + lane;
+            local = row - rbase;
+            tok = __ldg(p.perm + row) / p.k;
             if (local >= p.cap) {
-                if (lane == 0) report_error(p.status, kStCapacity, row, rank, (int)epoch);
-                continue;
+                report_error(p.status, kStCapacity, row, rank, (int)epoch);
+                tok = -1;
+            } else if (tok < 0 || tok >= p.T) {
+                report_error(p.status, kStDevice, -3, row, (int)epoch);
+                tok = -1;
             }
-            const int src = __ldg(p.perm + row) / p.k;
-            if (src < 0 || src >= p.T) {
-                if (lane == 0) report_error(p.status, kStDevice, -3, row, (int)epoch);
-                continue;
-            }
-            copy_row(reinterpret_cast<const uint4*>(p.x + (size_t)src * p.d),
-                     reinterpret_cast<uint4*>(p.recv[rank] + (size_t)local * p.d), nvec, lane);
         }
-        // publish: every lane orders its stores, then one arrival per unit
+        const uint4* src[kRowsPerChunk];
+        uint4* dst[kRowsPerChunk];
+#pragma unroll
+        for (int r = 0; r < kRowsPerChunk; ++r) {
+            const int tr = __shfl_sync(kFull, tok, r);
+            const int lr = __shfl_sync(kFull, local, r);
+            src[r] = tr >= 0 ? reinterpret_cast<const uint4*>(p.x + (size_t)tr * p.d) : nullptr;
+            dst[r] = tr >= 0 ? reinterpret_cast<uint4*>(p.recv[rank] + (size_t)lr * p.d) : nullptr;
+        }
+        for (int v0 = lane; v0 < nvec; v0 += 32 * kScatterVec) {
+            uint4 t[kRowsPerChunk][kScatterVec];
+#pragma unroll
+            for (int r = 0; r < kRowsPerChunk; ++r)
+#pragma unroll
+                for (int u = 0; u < kScatterVec; ++u)
+                    if (src[r] != nullptr && v0 + 32 * u < nvec) t[r][u] = __ldg(src[r] + v0 + 32 * u);
+#pragma unroll
+            for (int r = 0; r < kRowsPerChunk; ++r)
+#pragma unroll
+                for (int u = 0; u < kScatterVec; ++u)
+                    if (src[r] != nullptr && v0 + 32 * u < nvec) dst[r][v0 + 32 * u] = t[r][u];
+        }
         fence_proxy_async_global();
-        __threadfence();
         __syncwarp();
         if (lane == 0) {
+            const int m = j / kChunksPerTile;
+            const int mtile = mt_base[e] + m;
+            const int units_in_tile =
+                min(kChunksPerTile, (cnt + kRowsPerChunk - 1) / kRowsPerChunk - m * kChunksPerTile);
+            __threadfence();
             const uint32_t prev = atomicAdd(p.chunk_cnt + mtile, 1u);
-            if (prev == (uint32_t)(kChunksPerTile - 1)) {
+            if (prev + 1u == (uint32_t)units_in_tile) {
                 __threadfence();
                 p.chunk_cnt[mtile] = 0u;  // ready for the next call
                 fence_proxy_async_global();
@@ -237,7 +257,7 @@ struct Cfg {
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN);
     static constexpr int kTmemCols = 2 * BN;
     static constexpr size_t kSmem =
-        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + sizeof(int) * (kMaxE + 1);
+        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
     static_assert(BN == 128 || BN == 256, "tile_n");
 };
@@ -267,12 +287,19 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             ti.rows = -1;
         } else {
             const int u = (int)(tile / (uint32_t)p.n_tiles);
-            const int e = expert_of_mtile(mt_base, p.E, u);
+            const int e = expert_of(mt_base, p.E, u);
             const int mt_e = mt_base[e + 1] - mt_base[e];
             const int local = (int)(tile - (uint32_t)mt_base[e] * (uint32_t)p.n_tiles);
+            // bands of `band` row tiles (the last may be shorter); inside a band the
+            // column tile is the slow index, so a band's rows are needed first and
+            // each weight panel is reused by the band's row tiles while hot in L2
+            const int bh = p.band > 0 ? p.band : mt_e;
+            const int b = local / (bh * p.n_tiles);
+            const int rem = local - b * bh * p.n_tiles;
+            const int h = min(bh, mt_e - b * bh);
             ti.e = e;
-            ti.n = local / mt_e;
-            ti.m = local % mt_e;
+            ti.n = rem / h;
+            ti.m = b * bh + rem % h;
             ti.mtile = mt_base[e] + ti.m;
             const int seg0 = __ldg(p.offsets + e);
             const int cnt = __ldg(p.offsets + e + 1) - seg0;
@@ -434,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * C::kABytes;
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sB + STAGES * C::kBBytes);
-    int* mt_base = reinterpret_cast<int*>(ctl + 1);
+    int* mt_base = reinterpret_cast<int*>(ctl + 1);  // row tiles per expert, prefix
+    int* unit_base = mt_base + (kMaxE + 1);           // scatter units per expert, prefix
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -461,14 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_addr(&ctl->tmem_base), C::kTmemCols);
         tmem_relinquish();
     }
-    build_mtile_table(p.offsets, p.E, mt_base, ctl->wsum);  // contains __syncthreads
+    build_expert_table(p.offsets, p.E, kTileM, mt_base, ctl->wsum);  // contain __syncthreads
+    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum);
     if (mt_base[p.E] > p.max_mtiles || __ldg(p.offsets + p.E) != p.T * p.k) {
         // offsets that do not describe T*k rows: report, and schedule nothing
         __syncthreads();
         if (tid == 0) {
             report_error(p.status, kStDevice, -2, __ldg(p.offsets + p.E), 0);
-            mt_base[p.E] = 0;
-            for (int e = 0; e < p.E; ++e) mt_base[e] = 0;
+            for (int e = 0; e <= p.E; ++e) mt_base[e] = unit_base[e] = 0;
         }
         __syncthreads();
     }
@@ -482,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (role < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, role, epoch);
+        scatter_role(p, mt_base, unit_base, role, epoch);
         __syncthreads();
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }

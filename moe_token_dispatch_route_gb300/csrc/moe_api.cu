@@ -27,6 +27,7 @@ struct moe_plan_s {
     WorkspaceLayout ws{};
     long long timeout_ns = 0;
     int skip_publish = -1;
+    int band = 0;
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
     bool maps_valid = false;
@@ -189,6 +190,8 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->route_blocks = (p->T + kRouteChunk - 1) / kRouteChunk;
     p->timeout_ns = shape->timeout_ns != 0 ? shape->timeout_ns : kDefaultTimeoutNs;
     p->skip_publish = shape->debug_skip_publish > 0 ? shape->debug_skip_publish - 1 : -1;
+    // tuning override for sweeps only: row tiles per schedule band (0 = whole expert)
+    if (const char* env = std::getenv("MOE_TILE_BAND")) p->band = std::max(0, std::atoi(env));
 
     size_t off = kHdrBytes;
     p->ws.route_blk_off = off;
@@ -337,6 +340,7 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
     prm.producer_ctas = plan->producer_ctas;
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
+    prm.band = plan->band;
     if (launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
                              static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();

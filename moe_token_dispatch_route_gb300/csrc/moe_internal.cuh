@@ -84,6 +84,7 @@ struct DispatchGemmParams {
     int producer_ctas;
     int max_mtiles;                 // size of flags[] and chunk_cnt[]
     int skip_publish;               // m-tile whose flag is never published, or -1
+    int band;                       // row tiles per schedule band; 0 = the whole expert
 };
 
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
