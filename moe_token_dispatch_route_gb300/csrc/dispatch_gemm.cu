@@ -53,6 +53,18 @@ struct TileInfo {
     int arow;  // first row inside the rank's receive buffer
 };
 
+constexpr int kMaxPieceBufs = 8;
+
+// One staged piece of a destination row (scatter role): where it goes and
+// which 16-byte vectors of the row it holds.
+struct PieceRec {
+    uint16_t* dst;  // destination row in the rank buffer
+    int q0, q1;     // vector range [q0, q1) of the row
+    int e, j;       // expert and unit inside the expert
+    int flags;      // 1: row valid, 2: last piece of the unit
+    int pad;
+};
+
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
@@ -67,6 +79,7 @@ struct SmemCtl {
     int role;
     uint32_t epoch;
     int wsum[kThreads / 32];
+    PieceRec piece[kThreads / 32][kMaxPieceBufs];  // scatter: per-warp ring of staged pieces
 };
 
 struct Waiter {
@@ -165,88 +178,178 @@ __device__ __forceinline__ int expert_of(const int* table, int E, int u) {
 }
 
 // Scatter role: all 8 warps of a scatter CTA copy token rows into the rank
-// receive buffers with 16-byte loads and stores.
+// receive buffers.
 //
 // Work unit = up to 4 consecutive destination rows of one expert inside one
 // 128-row tile; only non-empty units exist (unit_base holds the per-expert
 // prefix of ceil(count/4)).  Units are visited in destination order, strided
 // over all scatter warps of all scatter CTAs, so the earliest tiles fill
-// first.  Each lane keeps 16 independent 16-byte loads in flight (4 rows x 4
-// vectors).  After a unit, lane 0 fences (cumulative over the warp's stores
-// through __syncwarp) and counts the unit in; the last unit of a tile
-// releases the tile's ready flag with the call's epoch.
-constexpr int kScatterVec = 4;
+// first.  Each row is split into pieces of at most 512 16-byte vectors.
+//
+// The loads are cp.async.cg (global -> shared, no L1 allocation) into a
+// lane-private staging area carved from the idle GEMM stage buffers (24 KB
+// per warp, split into 3-8 piece buffers), so the number of bytes in flight
+// is set by shared memory rather than by the small L1 left beside it.  A
+// warp keeps up to nbuf-1 pieces loading while it drains the oldest one
+// (shared -> registers -> global).  Each piece's destination is kept in a
+// per-warp ring in shared memory, so the drain needs no lookups.  After every
+// two finished units (and at the end) lane 0 fences, cumulative over the
+// warp's stores through __syncwarp, and counts the units in; the last unit of
+// a tile releases the tile's ready flag with the call's epoch.
+constexpr int kWarpSlotsPerLane = 48;  // 48 x 16 B per lane = 24 KB per warp
+constexpr int kPieceVecsMax = 512;
 
-__device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
-                             int role, uint32_t epoch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = p.producer_ctas * (kThreads / 32);
-    const int gw = role * (kThreads / 32) + warp;
-    const int total_units = unit_base[p.E];
+struct UnitCursor {
+    int c, stride, total;
+    int e, j, seg0, cnt, nrows, rank, rbase;
+    int r, q;       // row of the unit and piece of the row
+    int tok, local; // lane r (< nrows) holds row r's token (-1: skip the row) and rank-local row
+    bool done;
+};
+
+__device__ void cursor_load_unit(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base,
+                                 uint32_t epoch, int lane) {
+    u.done = u.c >= u.total;
+    if (u.done) return;
+    u.e = expert_of(unit_base, p.E, u.c);
+    u.j = u.c - unit_base[u.e];
+    u.seg0 = __ldg(p.offsets + u.e);
+    u.cnt = __ldg(p.offsets + u.e + 1) - u.seg0;
+    u.nrows = min(kRowsPerChunk, u.cnt - u.j * kRowsPerChunk);
     const int e_per_rank = p.E / p.R;
-    const int nvec = p.d / 8;
-    for (int c = gw; c < total_units; c += nwarps) {
-        const int e = expert_of(unit_base, p.E, c);
-        const int j = c - unit_base[e];  // unit inside the expert
-        const int seg0 = __ldg(p.offsets + e);
-        const int cnt = __ldg(p.offsets + e + 1) - seg0;
-        const int r_begin = j * kRowsPerChunk;
-        const int nrows = min(kRowsPerChunk, cnt - r_begin);
-        const int rank = e / e_per_rank;
-        const int rbase = __ldg(p.offsets + rank * e_per_rank);
-        // lane r < nrows looks up row r of the unit
-        int tok = -1, local = -1;
-        if (lane < nrows) {
-            const int row = seg0 + r_begin + lane;
-            local = row - rbase;
-            tok = __ldg(p.perm + row) / p.k;
-            if (local >= p.cap) {
-                report_error(p.status, kStCapacity, row, rank, (int)epoch);
-                tok = -1;
-            } else if (tok < 0 || tok >= p.T) {
-                report_error(p.status, kStDevice, -3, row, (int)epoch);
-                tok = -1;
-            }
-        }
-        const uint4* src[kRowsPerChunk];
-        uint4* dst[kRowsPerChunk];
-#pragma unroll
-        for (int r = 0; r < kRowsPerChunk; ++r) {
-            const int tr = __shfl_sync(kFull, tok, r);
-            const int lr = __shfl_sync(kFull, local, r);
-            src[r] = tr >= 0 ? reinterpret_cast<const uint4*>(p.x + (size_t)tr * p.d) : nullptr;
-            dst[r] = tr >= 0 ? reinterpret_cast<uint4*>(p.recv[rank] + (size_t)lr * p.d) : nullptr;
-        }
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kScatterVec) {
-            uint4 t[kRowsPerChunk][kScatterVec];
-#pragma unroll
-            for (int r = 0; r < kRowsPerChunk; ++r)
-#pragma unroll
-                for (int u = 0; u < kScatterVec; ++u)
-                    if (src[r] != nullptr && v0 + 32 * u < nvec) t[r][u] = __ldg(src[r] + v0 + 32 * u);
-#pragma unroll
-            for (int r = 0; r < kRowsPerChunk; ++r)
-#pragma unroll
-                for (int u = 0; u < kScatterVec; ++u)
-                    if (src[r] != nullptr && v0 + 32 * u < nvec) dst[r][v0 + 32 * u] = t[r][u];
-        }
-        fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) {
-            const int m = j / kChunksPerTile;
-            const int mtile = mt_base[e] + m;
-            const int units_in_tile =
-                min(kChunksPerTile, (cnt + kRowsPerChunk - 1) / kRowsPerChunk - m * kChunksPerTile);
-            __threadfence();
-            const uint32_t prev = atomicAdd(p.chunk_cnt + mtile, 1u);
-            if (prev + 1u == (uint32_t)units_in_tile) {
-                __threadfence();
-                p.chunk_cnt[mtile] = 0u;  // ready for the next call
-                fence_proxy_async_global();
-                if (mtile != p.skip_publish) st_release_gpu(p.flags + mtile, epoch);
-            }
+    u.rank = u.e / e_per_rank;
+    u.rbase = __ldg(p.offsets + u.rank * e_per_rank);
+    u.r = 0;
+    u.q = 0;
+    u.tok = -1;
+    u.local = -1;
+    if (lane < u.nrows) {
+        const int row = u.seg0 + u.j * kRowsPerChunk + lane;
+        u.local = row - u.rbase;
+        u.tok = __ldg(p.perm + row) / p.k;
+        if (u.local >= p.cap) {
+            report_error(p.status, kStCapacity, row, u.rank, (int)epoch);
+            u.tok = -1;
+        } else if (u.tok < 0 || u.tok >= p.T) {
+            report_error(p.status, kStDevice, -3, row, (int)epoch);
+            u.tok = -1;
         }
     }
+}
+
+__device__ void publish_unit(const DispatchGemmParams& p, const int* mt_base, int e, int j,
+                             uint32_t epoch) {
+    const int cnt = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    const int m = j / kChunksPerTile;
+    const int mtile = mt_base[e] + m;
+    const int units_in_tile =
+        min(kChunksPerTile, (cnt + kRowsPerChunk - 1) / kRowsPerChunk - m * kChunksPerTile);
+    const uint32_t prev = atomicAdd(p.chunk_cnt + mtile, 1u);
+    if (prev + 1u == (uint32_t)units_in_tile) {
+        __threadfence();
+        p.chunk_cnt[mtile] = 0u;  // ready for the next call
+        fence_proxy_async_global();
+        if (mtile != p.skip_publish) st_release_gpu(p.flags + mtile, epoch);
+    }
+}
+
+__device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
+                             int role, uint32_t epoch, uint8_t* staging, SmemCtl* ctl) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = p.producer_ctas * (kThreads / 32);
+    const int nvec = p.d / 8;
+    const int piece_vecs = min(nvec, kPieceVecsMax);
+    const int pieces_per_row = (nvec + piece_vecs - 1) / piece_vecs;
+    const int lane_slots = (piece_vecs + 31) / 32;  // 1..16
+    const int nbuf = min(kMaxPieceBufs, kWarpSlotsPerLane / lane_slots);  // 3..8
+    const uint32_t wslots = smem_addr(staging) + (uint32_t)(warp * kWarpSlotsPerLane * 32 * 16);
+    PieceRec* ring = ctl->piece[warp];
+
+    UnitCursor L;
+    L.c = role * (kThreads / 32) + warp;
+    L.stride = nwarps;
+    L.total = unit_base[p.E];
+    cursor_load_unit(L, p, unit_base, epoch, lane);
+
+    int pend_e[2], pend_j[2];
+    int npend = 0;
+    long long gi = 0, gd = 0;  // pieces issued, pieces drained
+    for (;;) {
+        // keep up to nbuf - 1 pieces loading
+        while (!L.done && gi - gd < nbuf - 1) {
+            const int b = (int)(gi % nbuf);
+            const int tr = __shfl_sync(kFull, L.tok, L.r);
+            const int lr = __shfl_sync(kFull, L.local, L.r);
+            const int q0 = L.q * piece_vecs;
+            const int q1 = min(q0 + piece_vecs, nvec);
+            if (tr >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)tr * p.d);
+                for (int i = 0; i < lane_slots; ++i) {
+                    const int v = q0 + lane + 32 * i;
+                    if (v < q1)
+                        cp_async16_cg(wslots + (uint32_t)(((b * lane_slots + i) * 32 + lane) * 16), src + v);
+                }
+            }
+            cp_async_commit();  // one group per piece (empty for a skipped row)
+            const bool last = L.q == pieces_per_row - 1 && L.r == L.nrows - 1;
+            if (lane == 0) {
+                PieceRec rec;
+                rec.dst = tr >= 0 ? p.recv[L.rank] + (size_t)lr * p.d : nullptr;
+                rec.q0 = q0;
+                rec.q1 = q1;
+                rec.e = L.e;
+                rec.j = L.j;
+                rec.flags = (tr >= 0 ? 1 : 0) | (last ? 2 : 0);
+                rec.pad = 0;
+                ring[b] = rec;
+            }
+            ++gi;
+            if (++L.q == pieces_per_row) {
+                L.q = 0;
+                if (++L.r == L.nrows) {
+                    L.c += L.stride;
+                    cursor_load_unit(L, p, unit_base, epoch, lane);
+                }
+            }
+        }
+        if (gd == gi) break;
+        // the oldest piece: wait for this lane's part, then store it
+        cp_async_wait_dyn((int)(gi - gd - 1));
+        __syncwarp();
+        const int b = (int)(gd % nbuf);
+        const PieceRec rec = ring[b];
+        if (rec.flags & 1) {
+            uint4* dst = reinterpret_cast<uint4*>(rec.dst);
+            for (int i = 0; i < lane_slots; ++i) {
+                const int v = rec.q0 + lane + 32 * i;
+                if (v < rec.q1) {
+                    uint4 t;
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(t.x), "=r"(t.y), "=r"(t.z), "=r"(t.w)
+                                 : "r"(wslots + (uint32_t)(((b * lane_slots + i) * 32 + lane) * 16)));
+                    dst[v] = t;
+                }
+            }
+        }
+        ++gd;
+        if (rec.flags & 2) {
+            pend_e[npend] = rec.e;
+            pend_j[npend] = rec.j;
+            ++npend;
+        }
+        if (npend == 2 || (L.done && gd == gi && npend > 0)) {
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                for (int i = 0; i < npend; ++i) publish_unit(p, mt_base, pend_e[i], pend_j[i], epoch);
+            }
+            npend = 0;
+        }
+    }
+    cp_async_wait<0>();
+    // the staging area becomes TMA (async-proxy) destination again
+    fence_proxy_async_smem();
 }
 
 template <int BN, int STAGES>
@@ -510,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (role < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, unit_base, role, epoch);
+        scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl);
         __syncthreads();
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }

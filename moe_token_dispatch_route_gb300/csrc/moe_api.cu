@@ -183,7 +183,7 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->num_ctas = shape->num_ctas != 0 ? std::min(shape->num_ctas, sms) : sms;
     const double scatter_bytes = (double)p->S * p->d * 2.0;
     int auto_p = (int)((scatter_bytes + (2 << 20) - 1) / (double)(2 << 20));
-    auto_p = std::max(8, std::min(auto_p, std::max(1, p->num_ctas / 4)));
+    auto_p = std::max(8, std::min(auto_p, std::max(1, p->num_ctas / 2)));
     p->producer_ctas = shape->producer_ctas != 0 ? shape->producer_ctas : auto_p;
     p->producer_ctas = std::max(1, std::min(p->producer_ctas, p->num_ctas));
     p->max_mtiles = (int)(p->S / kTileM) + p->E;
