@@ -90,12 +90,13 @@ typedef struct moe_shape {
 } moe_shape_t;
 
 typedef struct moe_plan_info {
-    int32_t tile_m, tile_n, tile_k;   /* GEMM tile (rows, columns, reduction step)      */
+    int32_t tile_m, tile_n, tile_k;   /* GEMM tile (rows, columns, reduction step); rows =
+                                         256 when CTA pairs share each tile                */
     int32_t stages;                   /* shared-memory pipeline depth                   */
     int32_t num_ctas, producer_ctas;  /* persistent grid and its initial scatter role   */
     int32_t sm_count;                 /* SMs of the plan's device                       */
     int32_t smem_bytes;               /* dynamic shared memory of the fused kernel      */
-    int32_t max_mtiles;               /* upper bound on row tiles: floor(S/tile_m) + E  */
+    int32_t max_mtiles;               /* upper bound on 128-row tiles: floor(S/128) + E */
     int32_t route_blocks;             /* CTAs of the routing kernel                     */
     int64_t workspace_bytes;          /* size moe_plan reported                         */
 } moe_plan_info_t;

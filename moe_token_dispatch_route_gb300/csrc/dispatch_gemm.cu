@@ -93,11 +93,14 @@ struct Waiter {
 // Bounded mbarrier wait.  Returns false if the CTA is aborting or the wait
 // exceeded the timeout (then it reports MOE_ERR_DEVICE and starts the abort).
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Waiter& w, int where,
-                         bool honor_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+                         bool honor_abort = true, bool cluster_scope = false) {
+    auto poll = [&]() {
+        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 127u) == 0) {
             if (honor_abort && *w.abort) return false;
             if (global_timer_ns() - t0 > (uint64_t)w.pipe_timeout_ns) {
@@ -656,6 +659,370 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair mode
+//
+// For layers with many rows per expert, CTAs run in clusters of two and every
+// GEMM tile is 256 rows x 256 columns, computed by tcgen05.mma.cta_group::2:
+// the even CTA of the pair (the leader) issues the MMAs, each CTA holds 128
+// rows of A and 128 of the 256 columns of B in its own shared memory, and each
+// CTA's TMEM receives its 128 rows of the accumulator.  Per SM this halves the
+// B operand traffic (TMA writes into shared memory and MMA reads from it).
+//  * The leader claims tiles and writes each tile's description into both
+//    CTAs' schedule rings (the peer's through distributed shared memory).
+//  * Both CTAs' TMA loads complete on the leader's stage barrier; the
+//    leader's MMA commit is multicast to both CTAs' stage-empty and
+//    accumulator-full barriers; both CTAs' epilogues release the accumulator
+//    on the leader's barrier.
+//  * Each CTA waits for the ready flag of its own 128-row half.
+// The scatter role is unchanged; a pair takes one role ticket and its two
+// CTAs become scatter CTAs 2t and 2t+1.
+template <int STAGES>
+struct PairCfg {
+    static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB: this CTA's 128 rows
+    static constexpr int kBBytes = 128 * kTileK * 2;     // 16 KB: this CTA's 128 columns
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBN = 256;                      // tile width of the pair
+    static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, kBN);
+    static constexpr int kTmemCols = 2 * kBN;            // two accumulators
+    static constexpr size_t kSmem =
+        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
+    static_assert(STAGES <= kMaxStages, "stages");
+};
+
+// tile description of one CTA's half of a pair tile
+__device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, int e, int m2,
+                               int n, int half, TileInfo& ti) {
+    const int e_per_rank = p.E / p.R;
+    const int seg0 = __ldg(p.offsets + e);
+    const int cnt = __ldg(p.offsets + e + 1) - seg0;
+    const int m = 2 * m2 + half;  // 128-row tile of this half
+    ti.e = e;
+    ti.m = m;
+    ti.n = n;
+    ti.row0 = seg0 + m * kTileM;
+    ti.rows = min(kTileM, cnt - m * kTileM);  // may be <= 0 for the odd half
+    ti.mtile = ti.rows > 0 ? mt_base[e] + m : -1;
+    ti.rank = e / e_per_rank;
+    ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
+}
+
+template <int STAGES>
+__device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
+                              const int* pt_base, uint8_t* sA, uint8_t* sB, const Waiter& w,
+                              bool leader, uint32_t peer) {
+    using C = PairCfg<STAGES>;
+    const uint32_t total_tiles = (uint32_t)pt_base[p.E] * (uint32_t)p.n_tiles;
+    tma_prefetch_map(&p.b_map);
+    for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
+    const uint32_t lead = leader ? cluster_ctarank() : peer;  // rank of the leader CTA
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int last_phase[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+    bool ok = true;
+    while (ok) {
+        TileInfo ti;
+        if (leader) {
+            if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 21, true, true)) break;
+            const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
+            TileInfo other;
+            if (tile >= total_tiles) {
+                ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = 0;
+                ti.e = -1;
+                other = ti;
+            } else {
+                const int u = (int)(tile / (uint32_t)p.n_tiles);
+                const int e = expert_of(pt_base, p.E, u);
+                const int pt_e = pt_base[e + 1] - pt_base[e];
+                const int local = (int)(tile - (uint32_t)pt_base[e] * (uint32_t)p.n_tiles);
+                const int n = local / pt_e;
+                const int m2 = local % pt_e;
+                pair_half_info(p, mt_base, e, m2, n, 0, ti);
+                pair_half_info(p, mt_base, e, m2, n, 1, other);
+            }
+            ctl->ring[slot] = ti;
+            const int* o = reinterpret_cast<const int*>(&other);
+            const uint32_t remote = mapa_shared(smem_addr(&ctl->ring[slot]), peer);
+#pragma unroll
+            for (int i = 0; i < (int)(sizeof(TileInfo) / 4); ++i) st_cluster_u32(remote + 4 * i, (uint32_t)o[i]);
+            mbar_arrive(smem_addr(&ctl->sfull[slot]));
+            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sfull[slot]), peer));
+        } else {
+            if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 22, true, true)) break;
+            ti = ctl->ring[slot];
+            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
+        }
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.e < 0) break;
+
+        if (ti.rows > 0) wait_flag(p.flags + ti.mtile, w, ti.mtile, ti.e);
+        fence_proxy_async_global();
+        const CUtensorMap* amap = &p.a_map[ti.rank];
+        const int brow = ti.e * p.d;
+        const int ncol = ti.n * C::kBN + (leader ? 0 : 128);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 23, true, true)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb_local = smem_addr(&ctl->full[stage]);
+            const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
+            tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, ti.arow);
+            tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes), &p.b_map, fb, ncol, brow + kb * kTileK);
+            tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192), &p.b_map, fb, ncol + 64,
+                             brow + kb * kTileK);
+            last_phase[stage] = (int)phase;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // the leader drains its stage barriers: each one completes only when both CTAs'
+    // loads of that stage have landed
+    if (leader) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s)
+            if (last_phase[s] >= 0)
+                wait_bar(smem_addr(&ctl->full[s]), (uint32_t)last_phase[s], w, 24, false, true);
+    }
+}
+
+template <int STAGES>
+__device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, uint8_t* sB,
+                              uint32_t tmem_base, const Waiter& w) {
+    using C = PairCfg<STAGES>;
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    while (ok) {
+        if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 25, true, true)) break;
+        const int e = ctl->ring[slot].e;
+        mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (e < 0) break;
+        if (!wait_bar(smem_addr(&ctl->tempty[acc]), aphase ^ 1u, w, 26, true, true)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kBN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 27, true, true)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+            const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(smem_addr(&ctl->tfull[acc]), 0x3);
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+    }
+    umma_commit_pair(smem_addr(&ctl->mma_done));
+    wait_bar(smem_addr(&ctl->mma_done), 0u, w, 28, false, true);
+}
+
+template <int STAGES>
+__device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
+                                   const Waiter& w, bool leader, uint32_t lead) {
+    using C = PairCfg<STAGES>;
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (;;) {
+        const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 29, true, true);
+        if (!__all_sync(kFull, got)) break;
+        const TileInfo ti = ctl->ring[slot];
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t se = smem_addr(&ctl->sempty[slot]);
+            if (leader) mbar_arrive(se);
+            else mbar_arrive_cluster(mapa_shared(se, lead));
+        }
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.e < 0) break;
+        const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 30, true, true);
+        if (!__all_sync(kFull, ready)) break;
+        tc_fence_after();
+        if (ti.rows > 0) {
+            const int r = 32 * q + lane;
+            const bool valid = r < ti.rows;
+            float* yrow = p.Y + (size_t)(ti.row0 + (valid ? r : 0)) * p.N + (size_t)ti.n * C::kBN;
+            const int ncols = min(C::kBN, p.N - ti.n * C::kBN);
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * C::kBN) + ((uint32_t)(32 * q) << 16);
+            for (int c = 0; c < ncols; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32(tbase + (uint32_t)c, v);
+                tmem_ld_wait(v);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        if (c + i < ncols)
+                            __stcs(reinterpret_cast<float4*>(yrow + c + i),
+                                   make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                               __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t te = smem_addr(&ctl->tempty[acc]);
+            if (leader) mbar_arrive(te);
+            else mbar_arrive_cluster(mapa_shared(te, lead));
+        }
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+    }
+}
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    dispatch_gemm_pair_kernel(const __grid_constant__ DispatchGemmParams p) {
+    using C = PairCfg<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * C::kABytes;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sB + STAGES * C::kBBytes);
+    int* mt_base = reinterpret_cast<int*>(ctl + 1);  // 128-row tiles per expert, prefix
+    int* unit_base = mt_base + (kMaxE + 1);           // scatter units per expert, prefix
+    int* pt_base = unit_base + (kMaxE + 1);           // 256-row pair tiles per expert, prefix
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank & 1u) == 0u;
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t lead = rank & ~1u;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);   // leader: its expect_tx arrival + both CTAs' bytes
+            mbar_init(smem_addr(&ctl->empty[s]), 1);  // the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&ctl->tfull[a]), 1);   // the leader's multicast commit
+            mbar_init(smem_addr(&ctl->tempty[a]), 8);  // leader: 4 + 4 epilogue warps
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(smem_addr(&ctl->sfull[r]), 1);
+            // leader: own MMA thread + 4 epilogue warps + the peer's TMA thread and 4 epilogue warps
+            mbar_init(smem_addr(&ctl->sempty[r]), 10);
+        }
+        mbar_init(smem_addr(&ctl->mma_done), 1);
+        ctl->abort = 0;
+        uint32_t ep = __ldcg(p.hdr + kHdrEpoch) + 1u;
+        ctl->epoch = ep == 0u ? 1u : ep;
+        mbar_fence_init();
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_addr(&ctl->tmem_base), C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    build_expert_table(p.offsets, p.E, kTileM, mt_base, ctl->wsum);  // contain __syncthreads
+    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum);
+    build_expert_table(p.offsets, p.E, 2 * kTileM, pt_base, ctl->wsum);
+    if (mt_base[p.E] > p.max_mtiles || __ldg(p.offsets + p.E) != p.T * p.k) {
+        __syncthreads();
+        if (tid == 0) {
+            report_error(p.status, kStDevice, -2, __ldg(p.offsets + p.E), 0);
+            for (int e = 0; e <= p.E; ++e) mt_base[e] = unit_base[e] = pt_base[e] = 0;
+        }
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs running, barrier inits and TMEM address visible to the pair
+    tc_fence_after();
+    // the pair's role ticket: taken by the leader, written into both CTAs
+    if (tid == 0 && leader) {
+        const int t = (int)atomicAdd(p.hdr + kHdrRoleCtr, 1u);
+        ctl->role = t;
+        st_cluster_u32(mapa_shared(smem_addr(&ctl->role), peer), (uint32_t)t);
+    }
+    cluster_sync_all();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint32_t epoch = ctl->epoch;
+    const int scatter_index = 2 * ctl->role + (int)(rank & 1u);
+
+    if (scatter_index < p.producer_ctas) {
+        unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
+        if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
+        scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl);
+        __syncthreads();
+        if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
+    }
+
+    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
+    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
+    if (warp == 0) {
+        if (lane == 0) pair_tma_role<STAGES>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && leader) pair_mma_role<STAGES>(p, ctl, sA, sB, tmem_base, w);
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        pair_epilogue_role<STAGES>(p, ctl, tmem_base, w, leader, lead);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still signal it
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    }
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.hdr + kHdrDoneCtr, 1u);
+        if (prev == gridDim.x - 1) {
+            __threadfence();
+            p.hdr[kHdrTileCtr] = 0u;
+            p.hdr[kHdrRoleCtr] = 0u;
+            p.hdr[kHdrDoneCtr] = 0u;
+            p.hdr[kHdrEpoch] = epoch;
+            unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
+            const unsigned long long inv = atomicExch(w64 + kHdrScatterInvStart / 2, 0ull);
+            const unsigned long long end = atomicExch(w64 + kHdrScatterEnd / 2, 0ull);
+            w64[kHdrLastScatterStart / 2] = ~inv;
+            w64[kHdrLastScatterEnd / 2] = end;
+            __threadfence();
+        }
+    }
+}
+
 template <int BN, int STAGES>
 cudaError_t launch_cfg(const DispatchGemmParams& p, int grid, size_t smem, cudaStream_t stream) {
     dispatch_gemm_kernel<BN, STAGES><<<grid, kThreads, smem, stream>>>(p);
@@ -663,6 +1030,25 @@ cudaError_t launch_cfg(const DispatchGemmParams& p, int grid, size_t smem, cudaS
 }
 
 }  // namespace
+
+size_t dispatch_gemm_pair_smem_bytes() { return PairCfg<6>::kSmem; }
+
+cudaError_t dispatch_gemm_pair_prepare(size_t smem, int* max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_gemm_pair_kernel<6>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    return cudaOccupancyMaxActiveClusters(max_clusters, dispatch_gemm_pair_kernel<6>, &cfg);
+}
+
+cudaError_t launch_dispatch_gemm_pair(const DispatchGemmParams& p, int grid, size_t smem,
+                                      cudaStream_t stream) {
+    dispatch_gemm_pair_kernel<6><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
 
 size_t dispatch_gemm_smem_bytes(int tile_n, int stages) {
     if (tile_n == 256 && stages == 4) return Cfg<256, 4>::kSmem;

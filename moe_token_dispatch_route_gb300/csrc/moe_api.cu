@@ -28,6 +28,7 @@ struct moe_plan_s {
     long long timeout_ns = 0;
     int skip_publish = -1;
     int band = 0;
+    bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
     bool maps_valid = false;
@@ -181,11 +182,30 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
         return MOE_ERR_UNSUPPORTED;
     }
     p->num_ctas = shape->num_ctas != 0 ? std::min(shape->num_ctas, sms) : sms;
+    // CTA pairs for layers with many rows per expert (on average at least one 256-row
+    // tile) and full-width tiles; MOE_PAIR=0/1 overrides the choice for tuning sweeps
+    p->pair = p->S >= 256LL * p->E && p->N >= 256 && (shape->tile_n == 0 || shape->tile_n == 256);
+    if (const char* env = std::getenv("MOE_PAIR")) p->pair = std::atoi(env) != 0 && p->N >= 256;
+    if (p->pair) {
+        int max_clusters = 0;
+        p->smem = dispatch_gemm_pair_smem_bytes();
+        if ((int)p->smem > smem_optin ||
+            dispatch_gemm_pair_prepare(p->smem, &max_clusters) != cudaSuccess || max_clusters < 1) {
+            cudaGetLastError();
+            p->pair = false;  // no co-resident pairs: keep the single-CTA kernel
+            p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
+        } else {
+            p->tile_n = 256;
+            p->stages = 6;
+            p->num_ctas = 2 * std::min(max_clusters, p->num_ctas / 2);
+        }
+    }
     const double scatter_bytes = (double)p->S * p->d * 2.0;
     int auto_p = (int)((scatter_bytes + (2 << 20) - 1) / (double)(2 << 20));
     auto_p = std::max(8, std::min(auto_p, std::max(1, p->num_ctas / 2)));
     p->producer_ctas = shape->producer_ctas != 0 ? shape->producer_ctas : auto_p;
     p->producer_ctas = std::max(1, std::min(p->producer_ctas, p->num_ctas));
+    if (p->pair) p->producer_ctas = std::min(p->num_ctas, (p->producer_ctas + 1) & ~1);  // whole pairs
     p->max_mtiles = (int)(p->S / kTileM) + p->E;
     p->route_blocks = (p->T + kRouteChunk - 1) / kRouteChunk;
     p->timeout_ns = shape->timeout_ns != 0 ? shape->timeout_ns : kDefaultTimeoutNs;
@@ -202,7 +222,7 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     off = round_up(off + (size_t)p->max_mtiles * 4, 256);
     p->ws.total = off;
 
-    if (dispatch_gemm_prepare_attributes(p->tile_n, p->stages, p->smem) != cudaSuccess ||
+    if ((!p->pair && dispatch_gemm_prepare_attributes(p->tile_n, p->stages, p->smem) != cudaSuccess) ||
         route_prepare_attributes() != cudaSuccess) {
         cudaGetLastError();
         delete p;
@@ -220,7 +240,7 @@ moe_status_t moe_plan_destroy(moe_plan_t plan) {
 
 moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info) {
     if (!plan || !info) return MOE_ERR_INVALID_ARG;
-    info->tile_m = kTileM;
+    info->tile_m = plan->pair ? 2 * kTileM : kTileM;
     info->tile_n = plan->tile_n;
     info->tile_k = kTileK;
     info->stages = plan->stages;
@@ -341,8 +361,11 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
-    if (launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
-                             static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    const cudaError_t lerr =
+        plan->pair ? launch_dispatch_gemm_pair(prm, plan->num_ctas, plan->smem, static_cast<cudaStream_t>(stream))
+                   : launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
+                                          static_cast<cudaStream_t>(stream));
+    if (lerr != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
