@@ -141,3 +141,59 @@ def test_receive_capacity_overflow_is_reported():
     inp = workloads.make_inputs(wl, seed=7)
     plan, bufs, rc, status = run_path(wl, inp, rank_capacity_rows=16)
     assert rc == binding.MOE_ERR_CAPACITY, status
+
+
+# ---------------------------------------------------------------- CTA-pair mode
+# The plan runs 256-row tiles on CTA pairs (tcgen05 cta_group::2) when experts
+# hold many rows; MOE_PAIR forces the choice either way for these tests.
+
+@pytest.mark.parametrize("T,d,E,k,N,R,bias", [
+    (1000, 128, 2, 1, 512, 1, "none"),    # 2 experts of ~500 rows: odd 128-row halves at the tail
+    (700, 256, 4, 2, 400, 2, "none"),     # ragged N tail (400 = 256 + 144), two ranks
+    (900, 128, 8, 2, 256, 4, "zipf"),     # skewed: some experts empty, some with < 128 rows
+    (130, 64, 1, 1, 272, 1, "none"),      # one expert, 130 rows: the odd half holds 2 rows
+])
+def test_pair_mode_full_parity(monkeypatch, T, d, E, k, N, R, bias):
+    monkeypatch.setenv("MOE_PAIR", "1")
+    plan, _ = _full_check(workloads.custom("pair", T, d, E, k, N, R, bias))
+    assert plan.info["tile_m"] == 256
+
+
+def test_pair_and_single_modes_agree(monkeypatch):
+    wl = workloads.custom("modes", 1200, 256, 4, 2, 512, 2, "none")
+    inp = workloads.make_inputs(wl, seed=8)
+    outs = {}
+    for mode in ("0", "1"):
+        monkeypatch.setenv("MOE_PAIR", mode)
+        plan, bufs, rc, status = run_path(wl, inp)
+        assert rc == 0, status
+        assert plan.info["tile_m"] == (256 if mode == "1" else 128)
+        outs[mode] = bufs.Y.cpu().double().numpy()
+    # same K order per element; the two MMA shapes may round differently, so compare to tolerance
+    err = np.abs(outs["0"] - outs["1"]).max()
+    assert err <= 1e-4 * np.sqrt(np.mean(outs["0"] ** 2))
+
+
+def test_pair_mode_role_split_does_not_change_bits(monkeypatch):
+    monkeypatch.setenv("MOE_PAIR", "1")
+    wl = workloads.custom("psplit", 1500, 128, 4, 2, 512, 1, "none")
+    inp = workloads.make_inputs(wl, seed=9)
+    outs = []
+    for kw in (dict(), dict(producer_ctas=2), dict(producer_ctas=60), dict(num_ctas=16, producer_ctas=4)):
+        _, bufs, rc, status = run_path(wl, inp, **kw)
+        assert rc == 0, status
+        outs.append(bufs.Y.clone())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+def test_pair_mode_missing_flag_times_out(monkeypatch):
+    monkeypatch.setenv("MOE_PAIR", "1")
+    wl = workloads.custom("pfault", 600, 128, 2, 1, 256, 1, "none")
+    inp = workloads.make_inputs(wl, seed=10)
+    plan, bufs, rc, status = run_path(wl, inp, timeout_ns=2_000_000, debug_skip_publish=2)
+    assert plan.info["tile_m"] == 256
+    assert rc == binding.MOE_ERR_TIMEOUT, status
+    assert status[1] == 1
+    plan2, bufs2, rc2, st2 = run_path(wl, inp)
+    assert rc2 == 0, st2
