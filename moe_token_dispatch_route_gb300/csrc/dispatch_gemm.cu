@@ -368,6 +368,12 @@ struct Cfg {
     static_assert(BN == 128 || BN == 256, "tile_n");
 };
 
+// The TMA thread claims the next tile, publishes its description to the MMA and
+// epilogue warps and reads its ready flag a few k-blocks before it has issued
+// the current tile, so the claim and flag latencies overlap the loads still
+// buffered ahead of the MMA.
+constexpr int kLookaheadKb = 4;
+
 template <int BN, int STAGES>
 __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
                          uint8_t* sA, uint8_t* sB, const Waiter& w) {
@@ -383,11 +389,11 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     int last_phase[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
-    bool ok = true;
-    while (ok) {
-        if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) break;
+
+    // claim a tile, describe it, hand it to the MMA and epilogue warps, read its flag
+    auto push_next = [&](TileInfo& ti, uint32_t& flag) -> bool {
+        if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
         const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
-        TileInfo ti;
         if (tile >= total_tiles) {
             ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = 0;
             ti.rows = -1;
@@ -420,21 +426,34 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             slot = 0;
             sphase ^= 1u;
         }
-        if (ti.rows < 0) break;
+        flag = ti.rows > 0 ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        return true;
+    };
 
-        wait_flag(p.flags + ti.mtile, w, ti.mtile, ti.e);
+    TileInfo cur;
+    uint32_t cur_flag = 0;
+    bool ok = push_next(cur, cur_flag);
+    while (ok && cur.rows >= 0) {
+        if (cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
         fence_proxy_async_global();
-        const CUtensorMap* amap = &p.a_map[ti.rank];
-        const int brow = ti.e * p.d;
-        const int ncol = ti.n * BN;
+        const CUtensorMap* amap = &p.a_map[cur.rank];
+        const int brow = cur.e * p.d;
+        const int ncol = cur.n * BN;
+        const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
+        TileInfo nxt;
+        uint32_t nxt_flag = 0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (kb == pre_kb && !push_next(nxt, nxt_flag)) {
+                ok = false;
+                break;
+            }
             if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 2)) {
                 ok = false;
                 break;
             }
             const uint32_t fb = smem_addr(&ctl->full[stage]);
             mbar_arrive_expect_tx(fb, C::kStageBytes);
-            tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, ti.arow);
+            tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
@@ -445,6 +464,8 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
                 phase ^= 1u;
             }
         }
+        cur = nxt;
+        cur_flag = nxt_flag;
     }
     // no TMA write may still be landing in shared memory when the CTA exits
 #pragma unroll
@@ -722,11 +743,15 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     int last_phase[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
-    bool ok = true;
-    while (ok) {
-        TileInfo ti;
+
+    // Leader: claim a pair tile and publish both halves' descriptions (the peer's
+    // through distributed shared memory).  Peer: take the next description from its
+    // ring; with `block` false it only takes one that is already there.  Both read
+    // the ready flag of their own half.
+    auto next_tile = [&](TileInfo& ti, uint32_t& flag, bool block, bool& got) -> bool {
+        got = false;
         if (leader) {
-            if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 21, true, true)) break;
+            if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 21, true, true)) return false;
             const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
             TileInfo other;
             if (tile >= total_tiles) {
@@ -751,7 +776,12 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             mbar_arrive(smem_addr(&ctl->sfull[slot]));
             mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sfull[slot]), peer));
         } else {
-            if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 22, true, true)) break;
+            const uint32_t sf = smem_addr(&ctl->sfull[slot]);
+            if (block) {
+                if (!wait_bar(sf, sphase, w, 22, true, true)) return false;
+            } else if (!mbar_try_wait_cluster(sf, sphase)) {
+                return true;  // not published yet
+            }
             ti = ctl->ring[slot];
             mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
         }
@@ -759,14 +789,33 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             slot = 0;
             sphase ^= 1u;
         }
-        if (ti.e < 0) break;
+        flag = (ti.e >= 0 && ti.rows > 0) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        got = true;
+        return true;
+    };
 
-        if (ti.rows > 0) wait_flag(p.flags + ti.mtile, w, ti.mtile, ti.e);
+    TileInfo cur;
+    uint32_t cur_flag = 0;
+    bool got = false;
+    bool ok = next_tile(cur, cur_flag, true, got);
+    while (ok && cur.e >= 0) {
+        if (cur.rows > 0 && cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
         fence_proxy_async_global();
-        const CUtensorMap* amap = &p.a_map[ti.rank];
-        const int brow = ti.e * p.d;
-        const int ncol = ti.n * C::kBN + (leader ? 0 : 128);
+        const CUtensorMap* amap = &p.a_map[cur.rank];
+        const int brow = cur.e * p.d;
+        const int ncol = cur.n * C::kBN + (leader ? 0 : 128);
+        const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
+        TileInfo nxt;
+        uint32_t nxt_flag = 0;
+        bool have_next = false;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!have_next && kb >= pre_kb) {
+                // the leader claims once at pre_kb; the peer polls from pre_kb on
+                if (!next_tile(nxt, nxt_flag, false, have_next)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 23, true, true)) {
                 ok = false;
                 break;
@@ -774,7 +823,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
             if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
-            tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, ti.arow);
+            tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes), &p.b_map, fb, ncol, brow + kb * kTileK);
             tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192), &p.b_map, fb, ncol + 64,
                              brow + kb * kTileK);
@@ -784,6 +833,10 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 phase ^= 1u;
             }
         }
+        if (!ok) break;
+        if (!have_next && !next_tile(nxt, nxt_flag, true, have_next)) break;
+        cur = nxt;
+        cur_flag = nxt_flag;
     }
     // the leader drains its stage barriers: each one completes only when both CTAs'
     // loads of that stage have landed
