@@ -11,7 +11,8 @@ namespace moe {
 
 // ---------------------------------------------------------------- constants
 
-constexpr int kRouteChunk = 64;     // tokens per routing CTA
+constexpr int kRouteChunk = 64;     // most tokens per routing CTA (8..64, a power of two)
+constexpr int kRouteFuseSlots = 8192;  // T*k up to this: the last routing CTA also permutes
 constexpr int kRouteThreads = 256;  // 8 warps
 
 constexpr int kTileM = 128;         // GEMM rows per tile (one UMMA M=128)
@@ -61,8 +62,13 @@ struct RouteArgs {
     uint32_t* hdr;
     int32_t* blk;     // [nb][E] per-CTA counts, then per-CTA bases
     int T, E, k, nb;
+    int chunk;        // tokens per CTA (set by launch_route)
+    int fuse_permute; // 1: the last CTA also writes dest and perm (set by launch_route)
 };
 
+// Routing CTAs for T tokens: tokens per CTA is the smallest of 8, 16, 32, 64 that
+// keeps the CTA count within the SM count (64 when none does).
+int route_blocks_for(int T, int sm_count);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t route_prepare_attributes();
 

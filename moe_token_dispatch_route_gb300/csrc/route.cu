@@ -9,7 +9,7 @@
 // and a destination order grouped by expert, then token, then slot.
 //
 // Two launches, no atomics that decide an order:
-//  1. route_select_kernel: one CTA per 64 tokens, one warp per token at a
+//  1. route_select_kernel: one CTA per 8-64 tokens, one warp per token at a
 //     time.  Each warp holds its token's E logits in registers (E/32 per
 //     lane), reduces max and sum-of-exp with xor shuffles and runs k rounds
 //     of a warp arg-max.  The CTA records which of its tokens picked each
@@ -18,6 +18,8 @@
 //     last CTA to finish (ticket counter) turns the per-CTA counts into the
 //     global offsets and per-CTA bases (a two-level exclusive scan).
 //  2. route_permute_kernel: dest = base[cta][e] + rank; perm[dest] = slot.
+//     For T*k <= 8192 the last CTA of the first kernel does this step itself
+//     and the second launch is skipped.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -86,7 +88,15 @@ __device__ void scan_counts(const RouteArgs& a) {
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int s = 0;
-        for (int b = b0; b < b1; ++b) s += __ldcg(a.blk + (size_t)b * E + e);
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {  // eight independent loads in flight
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(a.blk + (size_t)(b + u) * E + e);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        for (; b < b1; ++b) s += __ldcg(a.blk + (size_t)b * E + e);
         part[job] = s;
     }
     __syncthreads();
@@ -112,7 +122,18 @@ __device__ void scan_counts(const RouteArgs& a) {
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int run = tot[e] + part[job];
-        for (int b = b0; b < b1; ++b) {
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(a.blk + (size_t)(b + u) * E + e);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                a.blk[(size_t)(b + u) * E + e] = run;
+                run += v[u];
+            }
+        }
+        for (; b < b1; ++b) {
             int* p = a.blk + (size_t)b * E + e;
             const int c = __ldcg(p);
             *p = run;
@@ -132,8 +153,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
     for (int i = tid; i < E * kMaskWords; i += kRouteThreads) mask[i] = 0u;
     __syncthreads();
 
-    const int t0 = blockIdx.x * kRouteChunk;
-    const int ntok = min(kRouteChunk, a.T - t0);
+    const int chunk = a.chunk;
+    const int t0 = blockIdx.x * chunk;
+    const int ntok = min(chunk, a.T - t0);
     for (int tl = warp; tl < ntok; tl += kRouteThreads / 32) {
         const int t = t0 + tl;
         const float* L = a.logits + (size_t)t * E;
@@ -229,6 +251,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
     if (!s_last) return;
     __threadfence();
     scan_counts(a);
+    if (a.fuse_permute) {
+        // small batches: this CTA also turns every slot's rank into its destination row
+        __syncthreads();
+        const int S = a.T * a.k;
+        for (int s = tid; s < S; s += kRouteThreads) {
+            const int b = (s / a.k) / chunk;
+            const int e = __ldcg(a.topk_idx + s);
+            if (e < 0 || e >= E) continue;
+            const int pos = __ldcg(a.blk + (size_t)b * E + e) + __ldcg(a.dest + s);
+            a.dest[s] = pos;
+            if (pos >= 0 && pos < S) a.perm[pos] = s;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256) route_permute_kernel(const RouteArgs a) {
@@ -236,7 +271,7 @@ __global__ void __launch_bounds__(256) route_permute_kernel(const RouteArgs a) {
     for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < S;
          s += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(s / a.k);
-        const int b = t / kRouteChunk;
+        const int b = t / a.chunk;
         const int e = a.topk_idx[s];
         if (e < 0 || e >= a.E) continue;
         const int pos = a.blk[(size_t)b * a.E + e] + a.dest[s];
@@ -259,7 +294,21 @@ cudaError_t launch_select(const RouteArgs& a, cudaStream_t stream) {
 
 cudaError_t route_prepare_attributes() { return cudaSuccess; }  // < 48 KB dynamic smem
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
+int route_blocks_for(int T, int sm_count) {
+    int chunk = 8;
+    while (chunk < kRouteChunk && (T + chunk - 1) / chunk > sm_count) chunk *= 2;
+    return (T + chunk - 1) / chunk;
+}
+
+cudaError_t launch_route(const RouteArgs& args, cudaStream_t stream) {
+    // tokens per CTA: the power of two that gives exactly args.nb CTAs
+    RouteArgs a = args;
+    const int per = (a.T + a.nb - 1) / a.nb;
+    a.chunk = 1;
+    while (a.chunk < per) a.chunk *= 2;
+    if (a.chunk > kRouteChunk || (a.T + a.chunk - 1) / a.chunk != a.nb) return cudaErrorInvalidValue;
+    const long long S = (long long)a.T * a.k;
+    a.fuse_permute = S <= kRouteFuseSlots ? 1 : 0;
     cudaError_t err;
     if (a.E <= 32) err = launch_select<1>(a, stream);
     else if (a.E <= 64) err = launch_select<2>(a, stream);
@@ -267,8 +316,7 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
     else if (a.E <= 256) err = launch_select<8>(a, stream);
     else if (a.E <= 512) err = launch_select<16>(a, stream);
     else err = launch_select<32>(a, stream);
-    if (err != cudaSuccess) return err;
-    const long long S = (long long)a.T * a.k;
+    if (err != cudaSuccess || a.fuse_permute) return err;
     const int grid = (int)std::min<long long>((S + 255) / 256, 4096);
     route_permute_kernel<<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
