@@ -144,6 +144,13 @@ def algorithmic_work(wl, touched_experts: int):
     return flops, nbytes, scatter_bytes
 
 
+def launches_per_step(wl) -> int:
+    """Kernels of this library per step: routing select (+ permutation when
+    T*k > 8192; smaller batches permute inside the routing kernel) + the fused
+    dispatch/grouped-GEMM kernel."""
+    return 2 + (1 if wl.T * wl.k > 8192 else 0)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -162,62 +169,82 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def cpu_baseline(wl, rows=None):
-    """The CPU oracle, as it stands, on a bounded sample of the workload:
-    routing of all T tokens, then gather + fp64 grouped GEMM of the first
-    `rows` destination rows.  Returns (TFLOP/s on the sampled GEMM work, info)."""
-    import numpy as np
+class OracleSample:
+    """The CPU oracle, as it stands, on a bounded sample of one workload.
 
-    import oracle
-    from moe_token_dispatch_route_gb300 import workloads
+    One sample = routing of all T tokens (top-k, histogram, permutation), then
+    gather + fp64 grouped GEMM of the first `rows` destination rows.  Inputs and
+    the weight slice those rows need are prepared once, outside any timing."""
 
-    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
-    L = inp["logits"].numpy()
-    xb = workloads.bf16_bits(inp["x"])
-    if rows is None:
-        rows = 384  # about 10-20 s of single-core fp64 work on the Mixtral-shaped layer
-    t0 = time.perf_counter()
-    ref = oracle.route(L, wl.k)
-    t_route = time.perf_counter() - t0
-    sub = ref["perm"][:rows]
-    # experts covering the first `rows` destination rows
-    experts = sorted({oracle.expert_of_row(ref["offsets"], r) for r in range(rows)})
-    Ws = workloads.make_weights(workloads.custom("w", wl.T, wl.d, max(experts) + 1, 1, wl.N), seed=0)
-    Wb = workloads.bf16_bits(Ws)
-    off = np.minimum(ref["offsets"][: max(experts) + 2], rows).astype(np.int32)
-    t1 = time.perf_counter()
-    a_rows = oracle.gather(xb, sub, wl.k)
-    oracle.grouped_gemm(a_rows, Wb, off)
-    t_gemm = time.perf_counter() - t1
-    flops = 2.0 * rows * wl.d * wl.N
-    info = {"sample": f"routing of all {wl.T} tokens ({t_route:.2f} s) + gather and fp64 GEMM of the "
-                      f"first {rows} destination rows ({t_gemm:.2f} s); TFLOP/s over the sampled GEMM "
-                      f"FLOPs and the whole sample time", "cores": 1, "kind": "oracle"}
-    return flops / (t_route + t_gemm) / 1e12, info, t_route + t_gemm
+    def __init__(self, wl, max_rows=512):
+        import numpy as np
+
+        import oracle
+        from moe_token_dispatch_route_gb300 import workloads
+
+        self.wl = wl
+        self.oracle = oracle
+        inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+        self.L = inp["logits"].numpy()
+        self.xb = workloads.bf16_bits(inp["x"])
+        ref = oracle.route(self.L, wl.k)
+        rows = min(max_rows, wl.S)
+        experts = sorted({oracle.expert_of_row(ref["offsets"], r) for r in range(rows)})
+        self.n_exp = max(experts) + 1
+        W = workloads.make_weights(workloads.custom("w", wl.T, wl.d, self.n_exp, 1, wl.N), seed=0)
+        self.Wb = workloads.bf16_bits(W)
+        self.np = np
+
+    def run(self, rows):
+        """Time one sample; returns (seconds, GEMM FLOPs of the sample)."""
+        o, np = self.oracle, self.np
+        rows = min(rows, self.wl.S)
+        t0 = time.perf_counter()
+        ref = o.route(self.L, self.wl.k)
+        a_rows = o.gather(self.xb, ref["perm"][:rows], self.wl.k)
+        off = np.minimum(ref["offsets"][: self.n_exp + 1], rows).astype(np.int32)
+        o.grouped_gemm(a_rows, self.Wb[: self.n_exp], off)
+        secs = time.perf_counter() - t0
+        return secs, 2.0 * rows * self.wl.d * self.wl.N
+
+    def describe(self, rows, secs):
+        return {"sample": f"routing of all {self.wl.T} tokens + gather and fp64 GEMM of the first "
+                          f"{rows} destination rows, {secs:.2f} s; TFLOP/s = sampled GEMM FLOPs / "
+                          f"sample time", "cores": 1, "kind": "oracle"}
+
+
+def cpu_baseline(wl, rows=384):
+    """The oracle timed once on about 10-20 s of single-core work (384 rows on the
+    Mixtral-shaped layer); returns (TFLOP/s, info)."""
+    s = OracleSample(wl, max_rows=rows)
+    secs, flops = s.run(rows)
+    return flops / secs / 1e12, s.describe(rows, secs), secs
 
 
 def run_reference(args, wl):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
-    # each step: routing of all tokens + GEMM of a row sample sized so the run stays short
-    per_step_budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
-    rows = 8
-    val, info, secs = cpu_baseline(wl, rows=rows)
-    scale = max(1, min(512, int(rows * per_step_budget / max(secs, 1e-3))))
+    # each step is one oracle sample, sized so that warm-up + timed steps take about two minutes
+    sample = OracleSample(wl)
+    secs8, _ = sample.run(8)
+    per_step = max(0.2, 120.0 / max(1, args.steps + args.warmup))
+    rows = max(1, min(512, int(8 * per_step / max(secs8, 1e-4))))
+    for _ in range(args.warmup):
+        sample.run(rows)
     times = []
-    for i in range(args.warmup + args.steps):
-        v, info, secs = cpu_baseline(wl, rows=scale)
-        if i >= args.warmup:
-            times.append((v, secs))
-    value = statistics.median(v for v, _ in times)
-    ms = 1000.0 * statistics.median(s for _, s in times)
+    flops = 0.0
+    for _ in range(args.steps):
+        secs, flops = sample.run(rows)
+        times.append(secs)
+    total = sum(times)
+    value = len(times) * flops / total / 1e12
+    info = sample.describe(rows, statistics.median(times))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {**wl.describe(), "sample_rows_per_step": scale},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": info["sample"]},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {**wl.describe(), "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": UNIT, **info},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -355,7 +382,7 @@ def run_ours(args, wl):
         "touched_experts": touched,
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches_per_step(wl) * K,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

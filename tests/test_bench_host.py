@@ -1,0 +1,61 @@
+"""Host-side logic of bench.py without a GPU: the work model, the launch count,
+and the max-over-ranks aggregation across two gloo processes."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from moe_token_dispatch_route_gb300 import workloads
+
+
+def test_algorithmic_work_mixtral():
+    wl = workloads.WORKLOADS["mixtral"]
+    flops, nbytes, scatter = bench.algorithmic_work(wl, touched_experts=8)
+    assert flops == 2 * 8192 * 2 * 4096 * 14336
+    # x read, receive rows written and read back, Y written, 8 experts' weights read
+    assert nbytes == 8192 * 4096 * 2 + 2 * 16384 * 4096 * 2 + 16384 * 14336 * 4 + 8 * 4096 * 14336 * 2
+    assert scatter == 8192 * 4096 * 2 + 16384 * 4096 * 2
+    # tensor-bound: far above the ridge of ~280 FLOP/B
+    assert flops / nbytes > 800
+
+
+def test_launches_per_step():
+    assert bench.launches_per_step(workloads.WORKLOADS["mixtral"]) == 3
+    assert bench.launches_per_step(workloads.WORKLOADS["decode"]) == 2
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = bench.max_over_ranks(1.5 + rank, world)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_processes():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
