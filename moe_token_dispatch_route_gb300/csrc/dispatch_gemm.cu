@@ -199,7 +199,14 @@ __device__ __forceinline__ int expert_of(const int* table, int E, int u) {
 // two finished units (and at the end) lane 0 fences, cumulative over the
 // warp's stores through __syncwarp, and counts the units in; the last unit of
 // a tile releases the tile's ready flag with the call's epoch.
-constexpr int kWarpSlotsPerLane = 48;  // 48 x 16 B per lane = 24 KB per warp
+constexpr int kWarpSlotsPerLaneMax = 48;  // 48 x 16 B per lane = 24 KB per warp
+
+// 16-byte staging slots per lane that fit in a stage area of `bytes` (8 warps x 32 lanes)
+constexpr int scatter_slots_per_lane(size_t bytes) {
+    return (int)(bytes / ((kThreads / 32) * 32 * 16)) < kWarpSlotsPerLaneMax
+               ? (int)(bytes / ((kThreads / 32) * 32 * 16))
+               : kWarpSlotsPerLaneMax;
+}
 constexpr int kPieceVecsMax = 512;
 
 struct UnitCursor {
@@ -256,16 +263,19 @@ __device__ void publish_unit(const DispatchGemmParams& p, const int* mt_base, in
     }
 }
 
+// `slots_per_lane` 16-byte slots per lane of staging (at least 32, so that every warp has at
+// least two piece buffers), all inside the stage area
 __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
-                             int role, uint32_t epoch, uint8_t* staging, SmemCtl* ctl) {
+                             int role, uint32_t epoch, uint8_t* staging, SmemCtl* ctl,
+                             int slots_per_lane) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = p.producer_ctas * (kThreads / 32);
     const int nvec = p.d / 8;
     const int piece_vecs = min(nvec, kPieceVecsMax);
     const int pieces_per_row = (nvec + piece_vecs - 1) / piece_vecs;
     const int lane_slots = (piece_vecs + 31) / 32;  // 1..16
-    const int nbuf = min(kMaxPieceBufs, kWarpSlotsPerLane / lane_slots);  // 3..8
-    const uint32_t wslots = smem_addr(staging) + (uint32_t)(warp * kWarpSlotsPerLane * 32 * 16);
+    const int nbuf = min(kMaxPieceBufs, slots_per_lane / lane_slots);  // >= 1 when slots >= 16
+    const uint32_t wslots = smem_addr(staging) + (uint32_t)(warp * slots_per_lane * 32 * 16);
     PieceRec* ring = ctl->piece[warp];
 
     UnitCursor L;
@@ -366,6 +376,11 @@ struct Cfg {
         1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
     static_assert(BN == 128 || BN == 256, "tile_n");
+    // the scatter stages rows in the stage area: 8 warps x 32 lanes x slots x 16 B
+    static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
+    static_assert(kScatterSlots >= 32, "stage area too small for the scatter staging (two pieces per warp)");
+    static_assert((size_t)kScatterSlots * 16 * 32 * (kThreads / 32) <= (size_t)STAGES * kStageBytes,
+                  "scatter staging must stay inside the stage area");
 };
 
 // The TMA thread claims the next tile, publishes its description to the MMA and
@@ -637,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (role < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl);
+        scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl, C::kScatterSlots);
         __syncthreads();
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }
@@ -708,6 +723,10 @@ struct PairCfg {
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
+    static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
+    static_assert(kScatterSlots >= 32, "stage area too small for the scatter staging (two pieces per warp)");
+    static_assert((size_t)kScatterSlots * 16 * 32 * (kThreads / 32) <= (size_t)STAGES * kStageBytes,
+                  "scatter staging must stay inside the stage area");
 };
 
 // tile description of one CTA's half of a pair tile
@@ -1033,7 +1052,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (scatter_index < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl);
+        scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl, C::kScatterSlots);
         __syncthreads();
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }
