@@ -365,6 +365,36 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
     fence_proxy_async_smem();
 }
 
+// Epilogue staging: each epilogue warp turns a 32-row x 32-column fp32 block (one row per
+// lane, as tcgen05.ld 32x32b returns it) into row-contiguous 128-byte segments through a
+// padded shared-memory tile, so every store instruction writes 4 rows x 128 B instead of
+// 32 partial lines.  The row stride of 36 floats keeps the 16-byte writes and reads free
+// of bank conflicts.
+constexpr int kEpiStride = 36;
+constexpr int kEpiWarpFloats = 32 * kEpiStride;
+constexpr size_t kEpiBytes = (size_t)4 * kEpiWarpFloats * sizeof(float);  // 4 epilogue warps
+
+// `ybase`: the block's row 0, column 0 in Y; `ld`: Y's row stride in floats.
+__device__ __forceinline__ void store_block_rows(float* tile, const uint32_t (&v)[32], float* ybase,
+                                                 size_t ld, int rows_valid, int cols_valid, int lane) {
+    float4* mine = reinterpret_cast<float4*>(tile + lane * kEpiStride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        mine[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                              __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+    __syncwarp();
+    const int sub = lane >> 3;        // row within a group of 4
+    const int col = (lane & 7) * 4;   // first of this lane's 4 columns
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int row = 4 * j + sub;
+        if (row < rows_valid && col < cols_valid)
+            __stcs(reinterpret_cast<float4*>(ybase + (size_t)row * ld + col),
+                   *reinterpret_cast<const float4*>(tile + row * kEpiStride + col));
+    }
+    __syncwarp();
+}
+
 template <int BN, int STAGES>
 struct Cfg {
     static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB
@@ -373,7 +403,7 @@ struct Cfg {
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN);
     static constexpr int kTmemCols = 2 * BN;
     static constexpr size_t kSmem =
-        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
+        1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
     static_assert(BN == 128 || BN == 256, "tile_n");
     // the scatter stages rows in the stage area: 8 warps x 32 lanes x slots x 16 B
@@ -546,7 +576,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
 
 template <int BN, int STAGES>
 __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
-                              const Waiter& w) {
+                              const Waiter& w, float* epi) {
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter of this warp
     int slot = 0;
@@ -567,24 +597,15 @@ __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 9);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
-        const int r = 32 * q + lane;
-        const bool valid = r < ti.rows;
-        float* yrow = p.Y + (size_t)(ti.row0 + (valid ? r : 0)) * p.N + (size_t)ti.n * BN;
+        const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
+        float* ybase = p.Y + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * BN;
         const int ncols = min(BN, p.N - ti.n * BN);
         const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(32 * q) << 16);
         for (int c = 0; c < ncols; c += 32) {
             uint32_t v[32];
             tmem_ld_32x32(tbase + (uint32_t)c, v);
             tmem_ld_wait(v);
-            if (valid) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    if (c + i < ncols)
-                        __stcs(reinterpret_cast<float4*>(yrow + c + i),
-                               make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
-                }
-            }
+            if (rows_valid > 0) store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
         }
         tc_fence_before();
         mbar_arrive(smem_addr(&ctl->tempty[acc]));
@@ -602,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * C::kABytes;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sB + STAGES * C::kBBytes);
+    float* epi_tiles = reinterpret_cast<float*>(sB + STAGES * C::kBBytes);  // 4 x 32 x 36 fp32
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(epi_tiles) + kEpiBytes);
     int* mt_base = reinterpret_cast<int*>(ctl + 1);  // row tiles per expert, prefix
     int* unit_base = mt_base + (kMaxE + 1);           // scatter units per expert, prefix
 
@@ -666,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mma_role<BN, STAGES>(p, ctl, sA, sB, tmem_base, w);
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<BN, STAGES>(p, ctl, tmem_base, w);
+        epilogue_role<BN, STAGES>(p, ctl, tmem_base, w, epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
     }
 
     tc_fence_before();
@@ -721,7 +743,7 @@ struct PairCfg {
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, kBN);
     static constexpr int kTmemCols = 2 * kBN;            // two accumulators
     static constexpr size_t kSmem =
-        1024 + (size_t)STAGES * kStageBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
+        1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
     static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
     static_assert(kScatterSlots >= 32, "stage area too small for the scatter staging (two pieces per warp)");
@@ -921,7 +943,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
 
 template <int STAGES>
 __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
-                                   const Waiter& w, bool leader, uint32_t lead) {
+                                   const Waiter& w, bool leader, uint32_t lead, float* epi) {
     using C = PairCfg<STAGES>;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
@@ -947,25 +969,16 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 30, true, true);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
-        if (ti.rows > 0) {
-            const int r = 32 * q + lane;
-            const bool valid = r < ti.rows;
-            float* yrow = p.Y + (size_t)(ti.row0 + (valid ? r : 0)) * p.N + (size_t)ti.n * C::kBN;
+        const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
+        if (rows_valid > 0) {
+            float* ybase = p.Y + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * C::kBN;
             const int ncols = min(C::kBN, p.N - ti.n * C::kBN);
             const uint32_t tbase = tmem_base + (uint32_t)(acc * C::kBN) + ((uint32_t)(32 * q) << 16);
             for (int c = 0; c < ncols; c += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32(tbase + (uint32_t)c, v);
                 tmem_ld_wait(v);
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        if (c + i < ncols)
-                            __stcs(reinterpret_cast<float4*>(yrow + c + i),
-                                   make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                               __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
-                    }
-                }
+                store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
             }
         }
         tc_fence_before();
@@ -989,7 +1002,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * C::kABytes;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sB + STAGES * C::kBBytes);
+    float* epi_tiles = reinterpret_cast<float*>(sB + STAGES * C::kBBytes);  // 4 x 32 x 36 fp32
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(reinterpret_cast<uint8_t*>(epi_tiles) + kEpiBytes);
     int* mt_base = reinterpret_cast<int*>(ctl + 1);  // 128-row tiles per expert, prefix
     int* unit_base = mt_base + (kMaxE + 1);           // scatter units per expert, prefix
     int* pt_base = unit_base + (kMaxE + 1);           // 256-row pair tiles per expert, prefix
@@ -1066,7 +1080,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && leader) pair_mma_role<STAGES>(p, ctl, sA, sB, tmem_base, w);
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        pair_epilogue_role<STAGES>(p, ctl, tmem_base, w, leader, lead);
+        pair_epilogue_role<STAGES>(p, ctl, tmem_base, w, leader, lead,
+                                   epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
     }
 
     tc_fence_before();
