@@ -312,6 +312,20 @@ def run_ours(args, wl):
     total_s = sum(step_ms) / 1000.0
     total_s = max_over_ranks(total_s, world, dev)
 
+    # the step after the path (combine), timed on its own: reads Y, writes [T, N]
+    comb_out = torch.empty(wl.T, wl.N, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        binding.moe_combine(plan, bufs.Y, bufs.topk_w, bufs.dest, comb_out, stream)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for a_, b_ in cev:
+        flush.fill_(1.0)
+        a_.record(stream)
+        binding.moe_combine(plan, bufs.Y, bufs.topk_w, bufs.dest, comb_out, stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    combine_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in cev)
+    del comb_out
+
     # end to end through the same ABI: pinned host inputs in, Y out, every step
     x_h = inp["x"].pin_memory()
     l_h = inp["logits"].pin_memory()
@@ -380,6 +394,10 @@ def run_ours(args, wl):
                     "note": "first scatter CTA start to last scatter CTA end, last timed call; "
                             "runs concurrently with the GEMM CTAs"},
         "touched_experts": touched,
+        "combine": {"ms": combine_ms, "bytes": wl.S * wl.N * 4 + wl.T * wl.N * 4,
+                    "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
+                    "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,
+                    "note": "moe_combine (step after the path), timed separately; not in value"},
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step(wl) * K,

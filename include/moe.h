@@ -178,6 +178,21 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
                                void* workspace, int32_t* dev_status, void* stream);
 
 /*
+ * moe_combine -- the step after the path: undo the destination permutation and
+ * weight each token's k expert outputs by its gates.  The articles' table row
+ * "MoE Dispatch + GEMM" describes the dispatch side only; the combine is the
+ * mirror image that completes the layer's output.
+ *   Y      in:  fp32 [S][N] from moe_dispatch_gemm (destination order).
+ *   topk_w in:  fp32 [T][k] from moe_route.
+ *   dest   in:  int32 [S] from moe_route.
+ *   out    out: fp32 [T][N]; out[t][n] = sum_{j<k} topk_w[t][j] * Y[dest[t*k+j]][n],
+ *               fp32 fused multiply-adds in ascending j (identical on every run).
+ * Launches one kernel on `stream`; no workspace.
+ */
+MOE_API moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w,
+                                 const int32_t* dest, float* out, void* stream);
+
+/*
  * moe_read_status -- synchronise `stream`, copy the 4-word device status to
  * out[4] and return out[0] as a moe_status_t (MOE_ERR_CUDA if the copy or
  * the synchronisation fails).  This is the one call that waits for the GPU.

@@ -61,7 +61,7 @@ class PlanInfo(ctypes.Structure):
 
 
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
-            "moe_read_status", "moe_status_string", "moe_route_noalloc")
+            "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine")
 
 
 def load_library(path: str = LIB_PATH):
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
+    lib.moe_combine.argtypes = [VP] * 6
+    lib.moe_combine.restype = I32
     lib.moe_route_noalloc.argtypes = [VP] * 9
     lib.moe_route_noalloc.restype = I32
     lib.moe_status_string.argtypes = [I32]
@@ -175,6 +177,12 @@ def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, worksp
                                           _ptr(workspace), _ptr(dev_status),
                                           _stream(stream, plan.device))
     _check(rc, "moe_dispatch_gemm")
+
+
+def moe_combine(plan: Plan, Y, topk_w, dest, out, stream=None) -> None:
+    rc = load_library().moe_combine(plan.handle, _ptr(Y), _ptr(topk_w), _ptr(dest), _ptr(out),
+                                    _stream(stream, plan.device))
+    _check(rc, "moe_combine")
 
 
 def moe_read_status(dev_status, stream=None) -> tuple[int, list[int]]:

@@ -372,6 +372,31 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
     return MOE_OK;
 }
 
+moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w, const int32_t* dest,
+                         float* out, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (plan->T == 0) return MOE_OK;
+    if (!Y || !topk_w || !dest || !out || !aligned(Y, 16) || !aligned(out, 16) ||
+        !aligned(topk_w, 4) || !aligned(dest, 4))
+        return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return MOE_ERR_CUDA;
+    CombineArgs a;
+    a.Y = Y;
+    a.w = topk_w;
+    a.dest = dest;
+    a.out = out;
+    a.T = plan->T;
+    a.k = plan->k;
+    a.N = plan->N;
+    a.S = (int)plan->S;
+    if (launch_combine(a, plan->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 moe_status_t moe_read_status(const int32_t* dev_status, void* stream, int32_t out[4]) {
     if (!dev_status || !out) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -96,6 +96,15 @@ struct DispatchGemmParams {
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
                                  size_t smem, cudaStream_t stream);
 size_t dispatch_gemm_smem_bytes(int tile_n, int stages);
+struct CombineArgs {
+    const float* Y;       // [S][N] destination order
+    const float* w;       // [T][k] gate weights
+    const int32_t* dest;  // [T*k]
+    float* out;           // [T][N]
+    int T, k, N, S;
+};
+cudaError_t launch_combine(const CombineArgs& a, int sm_count, cudaStream_t stream);
+
 // CTA-pair mode (clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2)
 size_t dispatch_gemm_pair_smem_bytes();
 cudaError_t dispatch_gemm_pair_prepare(size_t smem, int* max_clusters);

@@ -14,4 +14,5 @@ from .oracle import (  # noqa: F401
     gemm_entry,
     expert_of_row,
     route,
+    combine,
 )

@@ -197,3 +197,22 @@ ORACLE_API int oracle_expert_of_row(const int32_t* offsets, int E, long row) {
         if (offsets[e] <= row && row < offsets[e + 1]) return e;
     return -1;
 }
+
+/*
+ * Combine (the step after the path): undo the permutation and weight each
+ * token's k expert outputs by its gates.
+ *   out[t][n] = sum_{j<k} w[t*k+j] * Y[dest[t*k+j]][n]
+ * summed in fp64, j ascending.  Y is [S][N] in destination order.
+ */
+ORACLE_API void oracle_combine(const double* Y, const double* w, const int32_t* dest,
+                               int T, int k, int N, double* out) {
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const long s = (long)t * k + j;
+                acc += w[s] * Y[(size_t)dest[s] * N + n];
+            }
+            out[(size_t)t * N + n] = acc;
+        }
+}

@@ -55,6 +55,8 @@ def _load():
             lib.oracle_grouped_gemm.restype = I
             lib.oracle_gemm_entry.argtypes = [P, P, I, I, I]
             lib.oracle_gemm_entry.restype = ctypes.c_double
+            lib.oracle_combine.argtypes = [P, P, P, I, I, I, P]
+            lib.oracle_combine.restype = None
             lib.oracle_expert_of_row.argtypes = [P, I, L]
             lib.oracle_expert_of_row.restype = I
             _lib = lib
@@ -158,3 +160,16 @@ def route(logits: np.ndarray, k: int):
     perm, dest = permutation(idx, E)
     return {"topk_idx": idx, "topk_w": w, "counts": counts, "offsets": offsets,
             "perm": perm, "dest": dest}
+
+
+def combine(Y: np.ndarray, topk_w: np.ndarray, dest: np.ndarray):
+    """Combine: out[t][n] = sum_j w[t,j] * Y[dest[t*k+j]][n] (fp64) -> [T, N]."""
+    Yd = np.ascontiguousarray(Y, dtype=np.float64)
+    w = np.ascontiguousarray(topk_w, dtype=np.float64)
+    T, k = w.shape
+    N = Yd.shape[1]
+    ds = np.ascontiguousarray(dest, dtype=np.int32).reshape(-1)
+    assert ds.shape[0] == T * k
+    out = np.empty((T, N), np.float64)
+    _load().oracle_combine(_p(Yd), _p(w), _p(ds), T, k, N, _p(out))
+    return out

@@ -27,6 +27,8 @@ MUTATIONS = {
                        "for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(We[((size_t)n * d + i) % ((size_t)d * N)]);"),
     # gather by slot index instead of token index
     "gather_index": ("int t = perm[row] / k;", "int t = perm[row] % T;"),
+    # combine weights indexed by token instead of slot
+    "combine_weight": ("acc += w[s] * Y[(size_t)dest[s] * N + n];", "acc += w[t] * Y[(size_t)dest[s] * N + n];"),
     # histogram off by one in the prefix sum
     "prefix": ("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
 }
@@ -76,6 +78,9 @@ def test_pins_catch_mutation(tmp_path, oracle_mod, name):
             lambda: pins.test_gather_is_fancy_index(o),
             lambda: pins.test_gemm_single_expert_is_plain_matmul(o),
             lambda: pins.test_gemm_uses_each_rows_own_expert(o),
+            lambda: pins.test_combine_single_slot_unit_gate_undoes_the_permutation(o),
+            lambda: pins.test_combine_matches_fancy_index_sum(o),
+            lambda: pins.test_combine_k_equals_e_with_constant_expert_outputs(o),
         ]
         caught = 0
         for c in checks:

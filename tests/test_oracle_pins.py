@@ -253,3 +253,41 @@ def test_gemm_within_fp64_summation_bound(oracle_mod):
             exact = sum(terms, Fraction(0))
             bound = gamma * float(sum(abs(t) for t in terms))
             assert abs(Fraction(Y[i, n]) - exact) <= Fraction(bound)
+
+
+# ---------------------------------------------------------------- combine (the step after the path)
+
+def test_combine_single_slot_unit_gate_undoes_the_permutation(oracle_mod):
+    rng = np.random.default_rng(20)
+    T, E, N = 30, 5, 12
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    r = oracle_mod.route(L, 1)
+    Y = rng.standard_normal((T, N))
+    out = oracle_mod.combine(Y, np.ones((T, 1)), r["dest"])
+    assert np.array_equal(out, Y[r["dest"]])
+    # and the permutation applied to token rows comes back to the token rows
+    rows_in_dest_order = Y[r["perm"]]
+    assert np.array_equal(oracle_mod.combine(rows_in_dest_order, np.ones((T, 1)), r["dest"]), Y)
+
+
+def test_combine_matches_fancy_index_sum(oracle_mod):
+    """A different implementation: numpy fancy indexing, then a weighted sum over slots."""
+    rng = np.random.default_rng(21)
+    T, E, k, N = 25, 7, 3, 9
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    r = oracle_mod.route(L, k)
+    Y = rng.standard_normal((T * k, N))
+    w = r["topk_w"]
+    out = oracle_mod.combine(Y, w, r["dest"])
+    ref = (Y[r["dest"].reshape(T, k)] * w[:, :, None]).sum(axis=1)
+    assert np.allclose(out, ref, rtol=1e-14, atol=1e-14)
+
+
+def test_combine_k_equals_e_with_constant_expert_outputs(oracle_mod):
+    """k = E and Y row = 1 for every slot: out = sum of all softmax weights = 1."""
+    rng = np.random.default_rng(22)
+    T, E, N = 10, 6, 4
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    r = oracle_mod.route(L, E)
+    out = oracle_mod.combine(np.ones((T * E, N)), r["topk_w"], r["dest"])
+    assert np.allclose(out, 1.0, rtol=0, atol=1e-13)
