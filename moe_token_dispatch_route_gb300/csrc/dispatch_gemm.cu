@@ -196,7 +196,7 @@ __device__ __forceinline__ int expert_of(const int* table, int E, int u) {
 // warp keeps up to nbuf-1 pieces loading while it drains the oldest one
 // (shared -> registers -> global).  Each piece's destination is kept in a
 // per-warp ring in shared memory, so the drain needs no lookups.  After every
-// two finished units (and at the end) lane 0 fences, cumulative over the
+// four finished units (and at the end) lane 0 fences, cumulative over the
 // warp's stores through __syncwarp, and counts the units in; the last unit of
 // a tile releases the tile's ready flag with the call's epoch.
 constexpr int kWarpSlotsPerLaneMax = 48;  // 48 x 16 B per lane = 24 KB per warp
@@ -208,6 +208,7 @@ constexpr int scatter_slots_per_lane(size_t bytes) {
                : kWarpSlotsPerLaneMax;
 }
 constexpr int kPieceVecsMax = 512;
+constexpr int kPublishBatch = 4;  // finished units per fence + publication
 
 struct UnitCursor {
     int c, stride, total;
@@ -284,7 +285,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
     L.total = unit_base[p.E];
     cursor_load_unit(L, p, unit_base, epoch, lane);
 
-    int pend_e[2], pend_j[2];
+    int pend_e[kPublishBatch], pend_j[kPublishBatch];
     int npend = 0;
     long long gi = 0, gd = 0;  // pieces issued, pieces drained
     for (;;) {
@@ -350,7 +351,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
             pend_j[npend] = rec.j;
             ++npend;
         }
-        if (npend == 2 || (L.done && gd == gi && npend > 0)) {
+        if (npend == kPublishBatch || (L.done && gd == gi && npend > 0)) {
             fence_proxy_async_global();
             __syncwarp();
             if (lane == 0) {
