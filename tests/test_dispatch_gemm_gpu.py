@@ -197,3 +197,11 @@ def test_pair_mode_missing_flag_times_out(monkeypatch):
     assert status[1] == 1
     plan2, bufs2, rc2, st2 = run_path(wl, inp)
     assert rc2 == 0, st2
+
+
+@pytest.mark.parametrize("T,d,E,k,N,R", [
+    (1024, 128, 1024, 8, 64, 32),   # the largest E and R the library accepts
+    (200, 64, 64, 32, 32, 4),       # the largest k
+])
+def test_limits_full_parity(T, d, E, k, N, R):
+    _full_check(workloads.custom("limits", T, d, E, k, N, R))
