@@ -326,6 +326,22 @@ def run_ours(args, wl):
     combine_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in cev)
     del comb_out
 
+    # the step before the path (GPU router logits), timed on its own: reads x and W_r
+    W_r = inp["W_r"].to(dev)
+    bias_d = inp["bias"].to(dev) if wl.bias != "none" else None
+    L_gpu = torch.empty_like(logits)
+    for _ in range(3):
+        binding.moe_router_logits(plan, x, W_r, bias_d, L_gpu, stream)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for a_, b_ in rev:
+        flush.fill_(1.0)
+        a_.record(stream)
+        binding.moe_router_logits(plan, x, W_r, bias_d, L_gpu, stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    router_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in rev)
+    del L_gpu
+
     # end to end through the same ABI: pinned host inputs in, Y out, every step
     x_h = inp["x"].pin_memory()
     l_h = inp["logits"].pin_memory()
@@ -394,6 +410,10 @@ def run_ours(args, wl):
                     "note": "first scatter CTA start to last scatter CTA end, last timed call; "
                             "runs concurrently with the GEMM CTAs"},
         "touched_experts": touched,
+        "router": {"ms": router_ms, "flops": 2.0 * wl.T * wl.d * wl.E,
+                   "tflops": 2.0 * wl.T * wl.d * wl.E / (router_ms * 1e9),
+                   "note": "moe_router_logits (step before the path; fp32 CUDA-core FMAs in a fixed "
+                           "order), timed separately; not in value"},
         "combine": {"ms": combine_ms, "bytes": wl.S * wl.N * 4 + wl.T * wl.N * 4,
                     "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
                     "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,

@@ -178,6 +178,22 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
                                void* workspace, int32_t* dev_status, void* stream);
 
 /*
+ * moe_router_logits -- the step before the path: the router logits that
+ * moe_route consumes, L = x @ W_r + bias, on the GPU.  The articles name no
+ * router; this library fixes its arithmetic so that routing stays bit-exact
+ * against a CPU reference: for each (token t, expert e) an fp32 accumulator
+ * runs fused multiply-adds over i ascending (each bf16 x bf16 product is exact
+ * in fp32), then the fp32 bias is added.  CUDA cores, no tensor cores.
+ *   x      in:  bf16 [T][d].
+ *   W_r    in:  bf16 [d][E] (E contiguous).
+ *   bias   in:  fp32 [E] or NULL.
+ *   logits out: fp32 [T][E].
+ * Launches one kernel on `stream`; no workspace.
+ */
+MOE_API moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_t* W_r,
+                                       const float* bias, float* logits, void* stream);
+
+/*
  * moe_combine -- the step after the path: undo the destination permutation and
  * weight each token's k expert outputs by its gates.  The articles' table row
  * "MoE Dispatch + GEMM" describes the dispatch side only; the combine is the

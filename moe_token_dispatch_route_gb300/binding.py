@@ -61,7 +61,8 @@ class PlanInfo(ctypes.Structure):
 
 
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
-            "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine")
+            "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
+            "moe_router_logits")
 
 
 def load_library(path: str = LIB_PATH):
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
+    lib.moe_router_logits.argtypes = [VP] * 6
+    lib.moe_router_logits.restype = I32
     lib.moe_combine.argtypes = [VP] * 6
     lib.moe_combine.restype = I32
     lib.moe_route_noalloc.argtypes = [VP] * 9
@@ -177,6 +180,12 @@ def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, worksp
                                           _ptr(workspace), _ptr(dev_status),
                                           _stream(stream, plan.device))
     _check(rc, "moe_dispatch_gemm")
+
+
+def moe_router_logits(plan: Plan, x, W_r, bias, logits, stream=None) -> None:
+    rc = load_library().moe_router_logits(plan.handle, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(logits),
+                                          _stream(stream, plan.device))
+    _check(rc, "moe_router_logits")
 
 
 def moe_combine(plan: Plan, Y, topk_w, dest, out, stream=None) -> None:

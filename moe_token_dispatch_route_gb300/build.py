@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "route.cu", "dispatch_gemm.cu", "route_noalloc.cu", "combine.cu"]
+SOURCES = ["moe_api.cu", "route.cu", "dispatch_gemm.cu", "route_noalloc.cu", "combine.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

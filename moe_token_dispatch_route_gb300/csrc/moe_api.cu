@@ -372,6 +372,30 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
     return MOE_OK;
 }
 
+moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_t* W_r,
+                               const float* bias, float* logits, void* stream) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (plan->T == 0) return MOE_OK;
+    if (!x || !W_r || !logits || !aligned(x, 4) || !aligned(W_r, 2) || !aligned(logits, 4) ||
+        (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return MOE_ERR_CUDA;
+    RouterArgs a;
+    a.x = x;
+    a.Wr = W_r;
+    a.bias = bias;
+    a.L = logits;
+    a.T = plan->T;
+    a.d = plan->d;
+    a.E = plan->E;
+    if (launch_router_logits(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w, const int32_t* dest,
                          float* out, void* stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;

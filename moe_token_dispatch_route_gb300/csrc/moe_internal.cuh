@@ -96,6 +96,15 @@ struct DispatchGemmParams {
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
                                  size_t smem, cudaStream_t stream);
 size_t dispatch_gemm_smem_bytes(int tile_n, int stages);
+struct RouterArgs {
+    const uint16_t* x;   // bf16 [T][d]
+    const uint16_t* Wr;  // bf16 [d][E]
+    const float* bias;   // fp32 [E] or null
+    float* L;            // fp32 [T][E]
+    int T, d, E;
+};
+cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream);
+
 struct CombineArgs {
     const float* Y;       // [S][N] destination order
     const float* w;       // [T][k] gate weights

@@ -15,4 +15,5 @@ from .oracle import (  # noqa: F401
     expert_of_row,
     route,
     combine,
+    router_logits,
 )

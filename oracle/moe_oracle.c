@@ -216,3 +216,24 @@ ORACLE_API void oracle_combine(const double* Y, const double* w, const int32_t* 
             out[(size_t)t * N + n] = acc;
         }
 }
+
+/*
+ * Router logits as this library's GPU router computes them (the step before
+ * the path): for each token t and expert e,
+ *   acc = 0; for i = 0..d-1 ascending: acc = fmaf(x[t][i], W_r[i][e], acc)
+ *   L[t][e] = acc + bias[e]          (fp32 add; bias may be NULL)
+ * fmaf is the correctly rounded fused multiply-add of C99 / IEEE 754, the
+ * same operation as the GPU's; a bf16 x bf16 product is exact in fp32, so
+ * each step is one rounding of (exact product + acc).
+ */
+ORACLE_API void oracle_router_logits(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                                     int T, int d, int E, float* L) {
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            float acc = 0.0f;
+            for (int i = 0; i < d; ++i)
+                acc = fmaf((float)bf16_to_double(x[(size_t)t * d + i]),
+                           (float)bf16_to_double(Wr[(size_t)i * E + e]), acc);
+            L[(size_t)t * E + e] = bias ? acc + bias[e] : acc;
+        }
+}

@@ -55,6 +55,8 @@ def _load():
             lib.oracle_grouped_gemm.restype = I
             lib.oracle_gemm_entry.argtypes = [P, P, I, I, I]
             lib.oracle_gemm_entry.restype = ctypes.c_double
+            lib.oracle_router_logits.argtypes = [P, P, P, I, I, I, P]
+            lib.oracle_router_logits.restype = None
             lib.oracle_combine.argtypes = [P, P, P, I, I, I, P]
             lib.oracle_combine.restype = None
             lib.oracle_expert_of_row.argtypes = [P, I, L]
@@ -172,4 +174,16 @@ def combine(Y: np.ndarray, topk_w: np.ndarray, dest: np.ndarray):
     assert ds.shape[0] == T * k
     out = np.empty((T, N), np.float64)
     _load().oracle_combine(_p(Yd), _p(w), _p(ds), T, k, N, _p(out))
+    return out
+
+
+def router_logits(x_bits: np.ndarray, Wr_bits: np.ndarray, bias=None):
+    """Router logits in the library's fixed fp32 order: fma over i ascending, then + bias."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(Wr_bits, dtype=np.uint16)
+    T, d = x.shape
+    E = W.shape[1]
+    out = np.empty((T, E), np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _load().oracle_router_logits(_p(x), _p(W), None if b is None else _p(b), T, d, E, _p(out))
     return out

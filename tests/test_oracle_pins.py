@@ -291,3 +291,32 @@ def test_combine_k_equals_e_with_constant_expert_outputs(oracle_mod):
     r = oracle_mod.route(L, E)
     out = oracle_mod.combine(np.ones((T * E, N)), r["topk_w"], r["dest"])
     assert np.allclose(out, 1.0, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- router logits (the step before the path)
+
+def test_router_logits_near_fp64_and_exact_on_small_integers(oracle_mod):
+    rng = np.random.default_rng(30)
+    T, d, E = 17, 96, 6
+    x = _bf16_bits_from_f32(rng.standard_normal((T, d)).astype(np.float32))
+    W = _bf16_bits_from_f32((rng.standard_normal((d, E)) / np.sqrt(d)).astype(np.float32))
+    L = oracle_mod.router_logits(x, W)
+    ref = _bits_to_f64(x) @ _bits_to_f64(W)
+    # fp32 sequential sum: error bounded by gamma_d * sum |terms| in fp32 arithmetic
+    bound = d * 2.0 ** -24 * (np.abs(_bits_to_f64(x)) @ np.abs(_bits_to_f64(W)))
+    assert np.all(np.abs(L - ref) <= bound)
+    # small integers: every partial sum is exact, so the result equals the exact dot product
+    xi = rng.integers(-8, 9, (T, d)).astype(np.float32)
+    Wi = rng.integers(-8, 9, (d, E)).astype(np.float32)
+    Li = oracle_mod.router_logits(_bf16_bits_from_f32(xi), _bf16_bits_from_f32(Wi))
+    assert np.array_equal(Li, (xi.astype(np.int64) @ Wi.astype(np.int64)).astype(np.float32))
+
+
+def test_router_logits_order_is_ascending_fma(oracle_mod):
+    """Terms 2^24, 1, -2^24: an ascending fp32 sum gives 0 (the 1 is absorbed);
+    any other grouping of these three gives 1."""
+    x = _bf16_bits_from_f32(np.array([[2.0 ** 12, 1.0, -(2.0 ** 12)]], np.float32))
+    W = _bf16_bits_from_f32(np.array([[2.0 ** 12], [1.0], [2.0 ** 12]], np.float32))
+    assert oracle_mod.router_logits(x, W)[0, 0] == 0.0
+    bias = np.array([0.5], np.float32)
+    assert oracle_mod.router_logits(x, W, bias)[0, 0] == 0.5

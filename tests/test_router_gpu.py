@@ -1,0 +1,71 @@
+"""moe_router_logits (the step before the path) against the oracle's router in
+the same fixed fp32 order: bit-exact logits, and bit-exact routing downstream."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_token_dispatch_route_gb300 import binding, workloads
+from tests.gpu_util import check_route
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_logits(wl, inp, rows=None):
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R)
+    x = inp["x"].cuda()
+    Wr = inp["W_r"].cuda()
+    bias = inp["bias"].cuda() if wl.bias != "none" else None
+    L = torch.full((wl.T, wl.E), float("nan"), dtype=torch.float32, device="cuda")
+    binding.moe_router_logits(plan, x, Wr, bias, L)
+    torch.cuda.synchronize()
+    return plan, L
+
+
+def _oracle_logits(wl, inp, rows=None):
+    xb = workloads.bf16_bits(inp["x"])
+    if rows is not None:
+        xb = np.ascontiguousarray(xb[rows])
+    bias = inp["bias"].numpy() if wl.bias != "none" else None
+    return oracle.router_logits(xb, workloads.bf16_bits(inp["W_r"]), bias)
+
+
+def _bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+@pytest.mark.parametrize("T,d,E,bias", [
+    (1, 64, 1, "none"), (100, 128, 3, "none"), (257, 256, 8, "none"), (300, 192, 17, "zipf"),
+    (64, 512, 128, "hot4"), (70, 64, 1024, "none"), (1000, 2048, 64, "zipf"),
+])
+def test_router_logits_bit_exact(T, d, E, bias):
+    wl = workloads.custom("router", T, d, E, 1, 16, 1, bias)
+    inp = workloads.make_inputs(wl, seed=14, with_weights=False)
+    _, L = _gpu_logits(wl, inp)
+    assert np.array_equal(_bits(L.cpu().numpy()), _bits(_oracle_logits(wl, inp)))
+
+
+def test_router_logits_mixtral_full():
+    wl = workloads.WORKLOADS["mixtral"]
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    _, L = _gpu_logits(wl, inp)
+    assert np.array_equal(_bits(L.cpu().numpy()), _bits(_oracle_logits(wl, inp)))
+
+
+def test_router_logits_deepseek_sampled_rows():
+    wl = workloads.WORKLOADS["deepseek_v3"]
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    _, L = _gpu_logits(wl, inp)
+    rows = np.array(sorted(set(range(0, 64)) | set(np.random.default_rng(1).integers(0, wl.T, 64).tolist()) | {wl.T - 1}))
+    assert np.array_equal(_bits(L.cpu().numpy()[rows]), _bits(_oracle_logits(wl, inp, rows)))
+
+
+@pytest.mark.parametrize("name", ["finegrained", "decode"])
+def test_gpu_router_then_route_matches_oracle_chain(name):
+    wl = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    plan, L = _gpu_logits(wl, inp)
+    bufs = binding.MoeBuffers(plan, "cuda")
+    binding.route(plan, L, bufs)
+    torch.cuda.synchronize()
+    check_route(bufs, oracle.route(_oracle_logits(wl, inp), wl.k), wl.k)
