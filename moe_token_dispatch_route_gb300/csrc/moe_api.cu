@@ -389,6 +389,7 @@ moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_
     a.T = plan->T;
     a.d = plan->d;
     a.E = plan->E;
+    a.sm_count = plan->sm_count;
     if (launch_router_logits(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;

@@ -102,6 +102,7 @@ struct RouterArgs {
     const float* bias;   // fp32 [E] or null
     float* L;            // fp32 [T][E]
     int T, d, E;
+    int sm_count;
 };
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream);
 
