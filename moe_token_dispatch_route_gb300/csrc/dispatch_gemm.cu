@@ -402,11 +402,11 @@ struct Cfg {
     static constexpr int kBBytes = BN * kTileK * 2;      // BN/64 boxes of 64 x 64
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN);
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;  // allocations are powers of two
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
-    static_assert(BN == 128 || BN == 256, "tile_n");
+    static_assert(BN == 128 || BN == 192 || BN == 256, "tile_n");
     // the scatter stages rows in the stage area: 8 warps x 32 lanes x slots x 16 B
     static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
     static_assert(kScatterSlots >= 32, "stage area too small for the scatter staging (two pieces per warp)");
@@ -1140,6 +1140,7 @@ cudaError_t launch_dispatch_gemm_pair(const DispatchGemmParams& p, int grid, siz
 
 size_t dispatch_gemm_smem_bytes(int tile_n, int stages) {
     if (tile_n == 256 && stages == 4) return Cfg<256, 4>::kSmem;
+    if (tile_n == 192 && stages == 4) return Cfg<192, 4>::kSmem;
     if (tile_n == 128 && stages == 6) return Cfg<128, 6>::kSmem;
     return 0;
 }
@@ -1147,6 +1148,9 @@ size_t dispatch_gemm_smem_bytes(int tile_n, int stages) {
 cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem) {
     if (tile_n == 256 && stages == 4)
         return cudaFuncSetAttribute(dispatch_gemm_kernel<256, 4>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (tile_n == 192 && stages == 4)
+        return cudaFuncSetAttribute(dispatch_gemm_kernel<192, 4>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (tile_n == 128 && stages == 6)
         return cudaFuncSetAttribute(dispatch_gemm_kernel<128, 6>,
@@ -1157,6 +1161,7 @@ cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages, size_t smem,
                                  cudaStream_t stream) {
     if (p.tile_n == 256 && stages == 4) return launch_cfg<256, 4>(p, grid, smem, stream);
+    if (p.tile_n == 192 && stages == 4) return launch_cfg<192, 4>(p, grid, smem, stream);
     if (p.tile_n == 128 && stages == 6) return launch_cfg<128, 6>(p, grid, smem, stream);
     return cudaErrorInvalidValue;
 }

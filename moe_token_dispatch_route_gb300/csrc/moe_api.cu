@@ -104,7 +104,7 @@ moe_status_t validate_shape(const moe_shape_t& s) {
     if (s.N % 16 != 0) return MOE_ERR_UNSUPPORTED;
     if (R > kMaxRanks || s.E % R != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s.T * s.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-    if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 256) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 192 && s.tile_n != 256) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -175,7 +175,7 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->S = (long long)p->T * p->k;
     p->cap = shape->rank_capacity_rows == 0 ? (int)p->S : shape->rank_capacity_rows;
     p->tile_n = shape->tile_n != 0 ? shape->tile_n : (p->N >= 256 ? 256 : 128);
-    p->stages = p->tile_n == 256 ? 4 : 6;
+    p->stages = p->tile_n == 128 ? 6 : 4;
     p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
     if (p->smem == 0 || (int)p->smem > smem_optin) {
         delete p;

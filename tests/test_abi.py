@@ -77,7 +77,7 @@ def _plan_rc(lib, **kw):
     (dict(N=24), binding.MOE_ERR_UNSUPPORTED),
     (dict(num_ranks=3), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=64, num_ranks=64), binding.MOE_ERR_UNSUPPORTED),
-    (dict(tile_n=192), binding.MOE_ERR_UNSUPPORTED),
+    (dict(tile_n=160), binding.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=2), binding.MOE_ERR_UNSUPPORTED),
 ])
 def test_plan_rejects_bad_shapes_before_any_device_call(lib, kw, expect):

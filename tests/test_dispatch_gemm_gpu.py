@@ -48,7 +48,7 @@ def test_edge_shapes_full_parity(T, d, E, k, N, R, bias):
     _full_check(workloads.custom("edge", T, d, E, k, N, R, bias))
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [128, 192, 256])
 def test_tile_widths(tile_n):
     _full_check(workloads.custom("tn", 700, 256, 8, 2, 1408 // 2, 1, "zipf"), tile_n=tile_n)
 
