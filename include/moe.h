@@ -68,6 +68,13 @@ typedef enum moe_status {
     MOE_ERR_DEVICE = 7        /* device: an internal pipeline wait gave up            */
 } moe_status_t;
 
+/* moe_shape_t.route_flags.  The expert choice is the same under every flag;
+ * only the gate weights differ.  RENORM alone is Mixtral-style gating (the
+ * softmax over the k chosen logits); SIGMOID | RENORM with a selection bias
+ * (moe_route_biased) is DeepSeek-V3-style gating. */
+#define MOE_ROUTE_RENORM 1
+#define MOE_ROUTE_SIGMOID 2
+
 /* Opaque host-side plan: shape, tile configuration and role split. */
 typedef struct moe_plan_s* moe_plan_t;
 
@@ -86,7 +93,10 @@ typedef struct moe_shape {
     int32_t debug_skip_publish; /* fault injection: 0 = off; m > 0 = never publish the
                                    ready flag of m-tile m-1 (the consumer's bounded wait
                                    then reports MOE_ERR_TIMEOUT)                         */
-    int32_t reserved;           /* must be 0                                            */
+    int32_t route_flags;        /* how moe_route scores the picks (gates); 0 = softmax
+                                   over all E logits.  MOE_ROUTE_SIGMOID: logistic of
+                                   each logit instead; MOE_ROUTE_RENORM: each token's k
+                                   gates divided by their sum.  Other bits must be 0.   */
 } moe_shape_t;
 
 typedef struct moe_plan_info {
@@ -131,8 +141,13 @@ MOE_API moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info);
  *   topk_idx out: int32 [T][k]; slot j holds the expert with the (j+1)-th
  *                 largest logit; between equal logits the lower expert index
  *                 comes first (-0.0 equals +0.0).
- *   topk_w   out: fp32 [T][k]; softmax over all E logits of the token,
- *                 evaluated at the chosen experts (not renormalised).
+ *   topk_w   out: fp32 [T][k]; the gate of each pick, from the chosen logit
+ *                 l: exp(l - max) / sum over all E of exp(logit - max) (default)
+ *                 or 1 / (1 + exp(-l)) (MOE_ROUTE_SIGMOID in the shape's
+ *                 route_flags); with MOE_ROUTE_RENORM each token's k gates are
+ *                 then divided by their sum.  fp32 with expf; with SIGMOID |
+ *                 RENORM a token whose chosen logits are all below about -87
+ *                 gets NaN gates (every logistic rounds to 0).
  *   counts   out: int32 [E]; rows routed to each expert.
  *   offsets  out: int32 [E+1]; exclusive prefix sum of counts, offsets[E] = S.
  *   perm     out: int32 [S]; destination row -> source slot t*k+j.  Rows are
@@ -147,6 +162,23 @@ MOE_API moe_status_t moe_route(moe_plan_t plan, const float* logits,
                        int32_t* counts, int32_t* offsets,
                        int32_t* perm, int32_t* dest,
                        void* workspace, void* stream);
+
+/*
+ * moe_route_biased -- moe_route with a per-expert selection bias: expert e of
+ * token t is ranked by the key fp32(logits[t][e] + selection_bias[e]) instead
+ * of the logit (same order rule, same tie rule), while the gates are computed
+ * from the unbiased logits as moe_route describes.  This is the bias that
+ * auxiliary-loss-free load balancing adjusts between steps: it moves tokens
+ * between experts without entering the weights the outputs are scaled by.
+ *   selection_bias in: fp32 [E] on the device, finite; NULL = moe_route.
+ * Other arguments, launches and errors as for moe_route.
+ */
+MOE_API moe_status_t moe_route_biased(moe_plan_t plan, const float* logits,
+                                      const float* selection_bias,
+                                      int32_t* topk_idx, float* topk_w,
+                                      int32_t* counts, int32_t* offsets,
+                                      int32_t* perm, int32_t* dest,
+                                      void* workspace, void* stream);
 
 /*
  * moe_dispatch_gemm -- the fused dispatch + per-expert grouped GEMM, one

@@ -29,6 +29,8 @@ MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_CAPACITY = 6
 MOE_ERR_DEVICE = 7
+MOE_ROUTE_RENORM = 1
+MOE_ROUTE_SIGMOID = 2
 
 
 class MoeError(RuntimeError):
@@ -44,7 +46,7 @@ class Shape(ctypes.Structure):
         ("rank_capacity_rows", ctypes.c_int32), ("tile_n", ctypes.c_int32),
         ("producer_ctas", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
         ("timeout_ns", ctypes.c_int64), ("debug_skip_publish", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("route_flags", ctypes.c_int32),
     ]
 
 
@@ -62,7 +64,7 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
             "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
-            "moe_router_logits")
+            "moe_router_logits", "moe_route_biased")
 
 
 def load_library(path: str = LIB_PATH):
@@ -84,6 +86,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_plan_info.restype = I32
     lib.moe_route.argtypes = [VP] * 10
     lib.moe_route.restype = I32
+    lib.moe_route_biased.argtypes = [VP] * 11
+    lib.moe_route_biased.restype = I32
     lib.moe_dispatch_gemm.argtypes = [VP] * 10
     lib.moe_dispatch_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
@@ -143,11 +147,11 @@ class Plan:
 def moe_plan(T: int, d: int, E: int, k: int, N: int, num_ranks: int = 1,
              rank_capacity_rows: int = 0, tile_n: int = 0, producer_ctas: int = 0,
              num_ctas: int = 0, timeout_ns: int = 0, debug_skip_publish: int = 0,
-             device: int | None = None) -> Plan:
+             route_flags: int = 0, device: int | None = None) -> Plan:
     lib = load_library()
     dev = torch.cuda.current_device() if device is None else int(device)
     shape = Shape(T, d, E, k, N, num_ranks, rank_capacity_rows, tile_n, producer_ctas, num_ctas,
-                  timeout_ns, debug_skip_publish, 0)
+                  timeout_ns, debug_skip_publish, route_flags)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib.moe_plan(ctypes.byref(shape), dev, ctypes.byref(handle), ctypes.byref(ws)), "moe_plan")
@@ -160,6 +164,16 @@ def moe_route(plan: Plan, logits, topk_idx, topk_w, counts, offsets, perm, dest,
                                   _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(dest),
                                   _ptr(workspace), _stream(stream, plan.device))
     _check(rc, "moe_route")
+
+
+def moe_route_biased(plan: Plan, logits, selection_bias, topk_idx, topk_w, counts, offsets, perm,
+                     dest, workspace, stream=None) -> None:
+    """moe_route ranking experts by logit + selection_bias[e]; gates from the logits."""
+    rc = load_library().moe_route_biased(plan.handle, _ptr(logits), _ptr(selection_bias),
+                                         _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                         _ptr(offsets), _ptr(perm), _ptr(dest), _ptr(workspace),
+                                         _stream(stream, plan.device))
+    _check(rc, "moe_route_biased")
 
 
 def moe_route_noalloc(plan: Plan, logits, topk_idx, topk_w, counts, offsets, perm, dest,
@@ -223,9 +237,9 @@ class MoeBuffers:
         self.status = torch.zeros(4, **i32)
 
 
-def route(plan: Plan, logits, bufs: MoeBuffers, stream=None):
-    moe_route(plan, logits, bufs.topk_idx, bufs.topk_w, bufs.counts, bufs.offsets, bufs.perm,
-              bufs.dest, bufs.workspace, stream)
+def route(plan: Plan, logits, bufs: MoeBuffers, stream=None, selection_bias=None):
+    moe_route_biased(plan, logits, selection_bias, bufs.topk_idx, bufs.topk_w, bufs.counts,
+                     bufs.offsets, bufs.perm, bufs.dest, bufs.workspace, stream)
 
 
 def dispatch_gemm(plan: Plan, x, W, bufs: MoeBuffers, stream=None):

@@ -96,7 +96,7 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 moe_status_t validate_shape(const moe_shape_t& s) {
     if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.N <= 0 || s.num_ranks < 0 ||
         s.rank_capacity_rows < 0 || s.producer_ctas < 0 || s.num_ctas < 0 || s.timeout_ns < 0 ||
-        s.debug_skip_publish < 0 || s.reserved != 0)
+        s.debug_skip_publish < 0 || (s.route_flags & ~(MOE_ROUTE_RENORM | MOE_ROUTE_SIGMOID)) != 0)
         return MOE_ERR_INVALID_ARG;
     const int R = s.num_ranks == 0 ? 1 : s.num_ranks;
     if (s.E > kMaxE || s.k > std::min(s.E, 32)) return MOE_ERR_UNSUPPORTED;
@@ -112,8 +112,10 @@ moe_status_t validate_shape(const moe_shape_t& s) {
 
 namespace moe {
 // Shape fields the routing launch needs, for entry points defined in other files.
-bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks, int* device) {
+bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks, int* device,
+                      int* route_flags) {
     if (!plan) return false;
+    *route_flags = plan->shape.route_flags;
     *T = plan->T;
     *E = plan->E;
     *k = plan->k;
@@ -257,7 +259,15 @@ moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info) {
 moe_status_t moe_route(moe_plan_t plan, const float* logits, int32_t* topk_idx, float* topk_w,
                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* dest,
                        void* workspace, void* stream) {
+    return moe_route_biased(plan, logits, nullptr, topk_idx, topk_w, counts, offsets, perm, dest,
+                            workspace, stream);
+}
+
+moe_status_t moe_route_biased(moe_plan_t plan, const float* logits, const float* selection_bias,
+                              int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                              int32_t* perm, int32_t* dest, void* workspace, void* stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;
+    if (selection_bias && !aligned(selection_bias, 4)) return MOE_ERR_INVALID_ARG;
     if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4))
         return MOE_ERR_INVALID_ARG;
     if (plan->T > 0 && (!logits || !topk_idx || !topk_w || !perm || !dest ||
@@ -291,6 +301,9 @@ moe_status_t moe_route(moe_plan_t plan, const float* logits, int32_t* topk_idx, 
     a.E = plan->E;
     a.k = plan->k;
     a.nb = plan->route_blocks;
+    a.sel_bias = selection_bias;
+    a.renorm = (plan->shape.route_flags & MOE_ROUTE_RENORM) ? 1 : 0;
+    a.sigmoid = (plan->shape.route_flags & MOE_ROUTE_SIGMOID) ? 1 : 0;
     if (launch_route(a, s) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;

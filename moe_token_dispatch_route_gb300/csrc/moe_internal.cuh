@@ -64,6 +64,9 @@ struct RouteArgs {
     int T, E, k, nb;
     int chunk;        // tokens per CTA (set by launch_route)
     int fuse_permute; // 1: the last CTA also writes dest and perm (set by launch_route)
+    const float* sel_bias;  // [E] added to the logits for selection only; nullptr: none
+    int renorm;       // 1: each token's gates are divided by their sum over the k picks
+    int sigmoid;      // 1: gate score = logistic(logit); 0: softmax over all E
 };
 
 // Routing CTAs for T tokens: tokens per CTA is the smallest of 8, 16, 32, 64 that

@@ -171,22 +171,29 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
                 v[i] = 0.f;
             }
         }
-        // softmax statistics over all E logits
-        float m = -INFINITY;
+        // softmax statistics over all E logits (unused by the logistic score)
+        float m = -INFINITY, s = 0.f;
+        if (!a.sigmoid) {
 #pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (live >> i & 1u) m = fmaxf(m, v[i]);
+            for (int i = 0; i < VPL; ++i)
+                if (live >> i & 1u) m = fmaxf(m, v[i]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-        float s = 0.f;
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
 #pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (live >> i & 1u) s += expf(v[i] - m);
+            for (int i = 0; i < VPL; ++i)
+                if (live >> i & 1u) s += expf(v[i] - m);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+        }
+        // selection keys: logit + bias (one fp32 add); the gates still use the logit
+        if (a.sel_bias) {
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (live >> i & 1u) v[i] += __ldg(a.sel_bias + lane + 32 * i);
+        }
 
         int my_e = -1;
-        float my_w = 0.f;
+        float my_v = 0.f;  // the pick's key; equal to its logit when there is no bias
         for (int j = 0; j < k; ++j) {
             float bv = 0.f;
             int be = INT_MAX;  // INT_MAX: nothing left in this lane
@@ -211,8 +218,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
             if ((be & 31) == lane) live &= ~(1u << (be >> 5));
             if (lane == j) {
                 my_e = be;
-                my_w = expf(bv - m) / s;
+                my_v = bv;
             }
+        }
+        float my_w = 0.f;
+        if (lane < k) {
+            const float lg = a.sel_bias ? __ldg(L + my_e) : my_v;
+            my_w = a.sigmoid ? 1.f / (1.f + expf(-lg)) : expf(lg - m) / s;
+        }
+        if (a.renorm) {  // divide by the sum of the token's k gates
+            float ws = my_w;  // 0 in lanes >= k
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(kFull, ws, off);
+            my_w = my_w / ws;
         }
         if (lane < k) {
             a.topk_idx[(size_t)t * k + lane] = my_e;

@@ -13,7 +13,8 @@
 #include "moe_internal.cuh"
 
 namespace moe {
-bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks, int* device);
+bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks, int* device,
+                      int* route_flags);
 }
 
 namespace {
@@ -54,8 +55,8 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 extern "C" moe_status_t moe_route_noalloc(moe_plan_t plan, const float* logits, int32_t* topk_idx,
                                           float* topk_w, int32_t* counts, int32_t* offsets,
                                           int32_t* perm, int32_t* dest, void* stream) {
-    int T = 0, E = 0, k = 0, nb = 0, device = 0;
-    if (!moe::plan_route_shape(plan, &T, &E, &k, &nb, &device)) return MOE_ERR_INVALID_ARG;
+    int T = 0, E = 0, k = 0, nb = 0, device = 0, flags = 0;
+    if (!moe::plan_route_shape(plan, &T, &E, &k, &nb, &device, &flags)) return MOE_ERR_INVALID_ARG;
     if ((size_t)nb * (size_t)E > kTableInts) return MOE_ERR_UNSUPPORTED;  // ceil(T/64)*E > 262144
     if (!counts || !offsets || !aligned4(counts) || !aligned4(offsets)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!logits || !topk_idx || !topk_w || !perm || !dest || !aligned4(logits) ||
@@ -89,6 +90,9 @@ extern "C" moe_status_t moe_route_noalloc(moe_plan_t plan, const float* logits, 
         a.E = E;
         a.k = k;
         a.nb = nb;
+        a.sel_bias = nullptr;
+        a.renorm = (flags & MOE_ROUTE_RENORM) ? 1 : 0;
+        a.sigmoid = (flags & MOE_ROUTE_SIGMOID) ? 1 : 0;
         // the ticket must start at zero; the per-CTA table is fully written before it is read
         if (cudaMemsetAsync(base, 0, kHeaderInts * sizeof(int32_t), s) != cudaSuccess ||
             moe::launch_route(a, s) != cudaSuccess)

@@ -6,6 +6,9 @@ CPU-baseline leg are the only users.  The product library never imports it.
 from .oracle import (  # noqa: F401
     build_oracle,
     topk,
+    renorm_gates,
+    select_biased,
+    gates_at,
     histogram,
     permutation,
     rank_base,

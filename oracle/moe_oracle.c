@@ -81,6 +81,106 @@ ORACLE_API int oracle_topk(const float* logits, int T, int E, int k,
 }
 
 /*
+ * Step A1, renormalised variant (Mixtral-style gating): the gates are the
+ * softmax over the k chosen logits only, so each token's k gates sum to 1.
+ *   topk_w[t*k+j] = exp(L[t][e_j] - M_t) / sum_{j'<k} exp(L[t][e_j'] - M_t)
+ * with e_j = topk_idx[t*k+j] (the picks of oracle_topk, unchanged) and M_t the
+ * largest chosen logit.  fp64, j' ascending.  Returns -1 on an index outside
+ * [0, E).
+ */
+ORACLE_API int oracle_topk_renorm_gates(const float* logits, int T, int E, int k,
+                                        const int32_t* topk_idx, double* topk_w) {
+    for (int t = 0; t < T; ++t) {
+        const float* L = logits + (size_t)t * E;
+        const int32_t* sel = topk_idx + (size_t)t * k;
+        for (int j = 0; j < k; ++j)
+            if (sel[j] < 0 || sel[j] >= E) return -1;
+        double M = (double)L[sel[0]];
+        for (int j = 1; j < k; ++j)
+            if ((double)L[sel[j]] > M) M = (double)L[sel[j]];
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += exp((double)L[sel[j]] - M);
+        for (int j = 0; j < k; ++j)
+            topk_w[(size_t)t * k + j] = exp((double)L[sel[j]] - M) / s;
+    }
+    return 0;
+}
+
+/*
+ * Step A1 with a selection-only bias (the bias that auxiliary-loss-free load
+ * balancing, as in DeepSeek-V3, moves between steps).  Expert e of token t is
+ * ranked by the key  key[e] = (float)(L[t][e] + bias[e])  -- one fp32 addition,
+ * rounded to nearest -- with the rule of oracle_topk on the keys (largest
+ * first, lower index between equal keys, -0.0 equal to +0.0).  Only topk_idx
+ * is produced; the gates come from the unbiased logits (oracle_gates_at).
+ * Returns -1 on a NaN key.
+ */
+ORACLE_API int oracle_select_biased(const float* logits, const float* bias, int T, int E, int k,
+                                    int32_t* topk_idx) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return -2;
+    float* key = (float*)malloc(sizeof(float) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!key || !taken) { free(key); free(taken); return -3; }
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; ++t) {
+        for (int e = 0; e < E; ++e) {
+            volatile float sum = logits[(size_t)t * E + e] + bias[e];  /* stored: rounded to fp32 */
+            key[e] = sum;
+            if (isnan(key[e])) rc = -1;
+        }
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || key[e] > key[best]) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+        }
+    }
+    free(key);
+    free(taken);
+    return rc;
+}
+
+/*
+ * Gates of given picks, from the unbiased logits, in fp64.
+ *   sigmoid = 0: softmax over all E logits evaluated at the pick,
+ *                exp(L[e_j] - m) / sum_e exp(L[e] - m), m the row maximum;
+ *   sigmoid = 1: the logistic 1 / (1 + exp(-L[e_j])).
+ *   renorm  = 1: then each token's k gates are divided by their sum
+ *                (j ascending).
+ * Returns -1 on an index outside [0, E).
+ */
+ORACLE_API int oracle_gates_at(const float* logits, const int32_t* topk_idx, int T, int E, int k,
+                               int sigmoid, int renorm, double* topk_w) {
+    for (int t = 0; t < T; ++t) {
+        const float* L = logits + (size_t)t * E;
+        const int32_t* sel = topk_idx + (size_t)t * k;
+        double* w = topk_w + (size_t)t * k;
+        for (int j = 0; j < k; ++j)
+            if (sel[j] < 0 || sel[j] >= E) return -1;
+        if (sigmoid) {
+            for (int j = 0; j < k; ++j) w[j] = 1.0 / (1.0 + exp(-(double)L[sel[j]]));
+        } else {
+            double m = (double)L[0];
+            for (int e = 1; e < E; ++e)
+                if ((double)L[e] > m) m = (double)L[e];
+            double s = 0.0;
+            for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);
+            for (int j = 0; j < k; ++j) w[j] = exp((double)L[sel[j]] - m) / s;
+        }
+        if (renorm) {
+            double z = 0.0;
+            for (int j = 0; j < k; ++j) z += w[j];
+            for (int j = 0; j < k; ++j) w[j] /= z;
+        }
+    }
+    return 0;
+}
+
+/*
  * Step A2: per-expert histogram and its exclusive prefix sum.
  * counts[e] = number of (t, j) with topk_idx[t*k+j] == e;
  * offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e].

@@ -43,6 +43,12 @@ def _load():
             L = ctypes.c_long
             lib.oracle_topk.argtypes = [P, I, I, I, P, P]
             lib.oracle_topk.restype = I
+            lib.oracle_topk_renorm_gates.argtypes = [P, I, I, I, P, P]
+            lib.oracle_topk_renorm_gates.restype = I
+            lib.oracle_select_biased.argtypes = [P, P, I, I, I, P]
+            lib.oracle_select_biased.restype = I
+            lib.oracle_gates_at.argtypes = [P, P, I, I, I, I, I, P]
+            lib.oracle_gates_at.restype = I
             lib.oracle_histogram.argtypes = [P, I, I, I, P, P]
             lib.oracle_histogram.restype = I
             lib.oracle_permutation.argtypes = [P, I, I, I, P, P]
@@ -80,6 +86,47 @@ def topk(logits: np.ndarray, k: int):
     if rc != 0:
         raise ValueError(f"oracle_topk failed ({rc})")
     return idx, w
+
+
+def renorm_gates(logits: np.ndarray, topk_idx: np.ndarray):
+    """Step A1, renormalised variant: softmax over each token's k chosen logits
+    -> topk_w float64 [T,k]."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, E = L.shape
+    k = idx.shape[1]
+    assert idx.shape[0] == T
+    w = np.empty((T, k), np.float64)
+    if _load().oracle_topk_renorm_gates(_p(L), T, E, k, _p(idx), _p(w)) != 0:
+        raise ValueError("expert index out of range")
+    return w
+
+
+def select_biased(logits: np.ndarray, bias: np.ndarray, k: int):
+    """Step A1 ranked by the fp32 key logit + bias[e] -> topk_idx int32 [T,k]."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    b = np.ascontiguousarray(bias, dtype=np.float32)
+    T, E = L.shape
+    assert b.shape == (E,)
+    idx = np.empty((T, k), np.int32)
+    rc = _load().oracle_select_biased(_p(L), _p(b), T, E, k, _p(idx))
+    if rc != 0:
+        raise ValueError(f"oracle_select_biased failed ({rc})")
+    return idx
+
+
+def gates_at(logits: np.ndarray, topk_idx: np.ndarray, sigmoid: bool = False,
+             renorm: bool = False):
+    """Gates of the given picks from the logits (softmax over all E, or the
+    logistic), optionally divided by their per-token sum -> float64 [T,k]."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, E = L.shape
+    k = idx.shape[1]
+    w = np.empty((T, k), np.float64)
+    if _load().oracle_gates_at(_p(L), _p(idx), T, E, k, int(sigmoid), int(renorm), _p(w)) != 0:
+        raise ValueError("expert index out of range")
+    return w
 
 
 def histogram(topk_idx: np.ndarray, E: int):
@@ -154,10 +201,20 @@ def expert_of_row(offsets: np.ndarray, row: int) -> int:
     return int(_load().oracle_expert_of_row(_p(off), off.shape[0] - 1, int(row)))
 
 
-def route(logits: np.ndarray, k: int):
-    """Steps A1-A3 chained: returns a dict of the oracle's routing outputs."""
+def route(logits: np.ndarray, k: int, renorm: bool = False, sigmoid: bool = False,
+          selection_bias=None):
+    """Steps A1-A3 chained: returns a dict of the oracle's routing outputs.
+    renorm: each token's gates divided by their sum over the k picks (for the
+    softmax: the softmax over the k chosen logits); sigmoid: logistic gates;
+    selection_bias: [E] added to the logits for the choice only."""
     E = logits.shape[1]
     idx, w = topk(logits, k)
+    if selection_bias is not None:
+        idx = select_biased(logits, selection_bias, k)
+    if sigmoid or selection_bias is not None:
+        w = gates_at(logits, idx, sigmoid=sigmoid, renorm=renorm)
+    elif renorm:
+        w = renorm_gates(logits, idx)
     counts, offsets = histogram(idx, E)
     perm, dest = permutation(idx, E)
     return {"topk_idx": idx, "topk_w": w, "counts": counts, "offsets": offsets,

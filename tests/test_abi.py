@@ -56,7 +56,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 def _plan_rc(lib, **kw):
     fields = dict(T=64, d=128, E=8, k=2, N=256, num_ranks=1, rank_capacity_rows=0, tile_n=0,
-                  producer_ctas=0, num_ctas=0, timeout_ns=0, debug_skip_publish=0, reserved=0)
+                  producer_ctas=0, num_ctas=0, timeout_ns=0, debug_skip_publish=0, route_flags=0)
     fields.update(kw)
     shape = binding.Shape(**fields)
     h = ctypes.c_void_p()
@@ -68,7 +68,7 @@ def _plan_rc(lib, **kw):
     (dict(T=-1), binding.MOE_ERR_INVALID_ARG),
     (dict(d=0), binding.MOE_ERR_INVALID_ARG),
     (dict(k=0), binding.MOE_ERR_INVALID_ARG),
-    (dict(reserved=1), binding.MOE_ERR_INVALID_ARG),
+    (dict(route_flags=4), binding.MOE_ERR_INVALID_ARG),
     (dict(debug_skip_publish=-2), binding.MOE_ERR_INVALID_ARG),
     (dict(E=1025, k=2), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=8, k=9), binding.MOE_ERR_UNSUPPORTED),
@@ -90,6 +90,7 @@ def test_null_arguments_are_rejected(lib):
     assert lib.moe_plan(None, 0, ctypes.byref(h), ctypes.byref(ws)) == binding.MOE_ERR_INVALID_ARG
     nulls = [None] * 10
     assert lib.moe_route(*nulls) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_biased(*([None] * 11)) == binding.MOE_ERR_INVALID_ARG
     assert lib.moe_dispatch_gemm(*nulls) == binding.MOE_ERR_INVALID_ARG
     out = (ctypes.c_int32 * 4)()
     assert lib.moe_read_status(None, None, out) == binding.MOE_ERR_INVALID_ARG

@@ -20,8 +20,11 @@ MUTATIONS = {
     "perm_order": ("for (int t = 0; t < T; ++t)\n            for (int j = 0; j < k; ++j)\n                if (topk_idx",
                    "for (int j = 0; j < k; ++j)\n            for (int t = 0; t < T; ++t)\n                if (topk_idx"),
     # softmax denominator drops one term
-    "softmax_sum": ("for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);",
-                    "for (int e = 1; e < E; ++e) s += exp((double)L[e] - m);"),
+    "softmax_sum": ("\n        for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);",
+                    "\n        for (int e = 1; e < E; ++e) s += exp((double)L[e] - m);"),
+    # the same slip in the gates of given picks
+    "gates_softmax_sum": ("\n            for (int e = 0; e < E; ++e) s += exp((double)L[e] - m);",
+                          "\n            for (int e = 1; e < E; ++e) s += exp((double)L[e] - m);"),
     # transposed weight operand
     "gemm_transpose": ("const uint16_t* wrow = We + (size_t)i * N;\n                for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(wrow[n]);",
                        "for (int n = 0; n < N; ++n) acc[n] += a * bf16_to_double(We[((size_t)n * d + i) % ((size_t)d * N)]);"),
@@ -29,6 +32,21 @@ MUTATIONS = {
     "gather_index": ("int t = perm[row] / k;", "int t = perm[row] % T;"),
     # combine weights indexed by token instead of slot
     "combine_weight": ("acc += w[s] * Y[(size_t)dest[s] * N + n];", "acc += w[t] * Y[(size_t)dest[s] * N + n];"),
+    # renormalised gates: denominator drops the first pick
+    "renorm_sum": ("for (int j = 0; j < k; ++j) s += exp((double)L[sel[j]] - M);",
+                   "for (int j = 1; j < k; ++j) s += exp((double)L[sel[j]] - M);"),
+    # renormalised gates: numerator taken from the wrong slot
+    "renorm_slot": ("topk_w[(size_t)t * k + j] = exp((double)L[sel[j]] - M) / s;",
+                    "topk_w[(size_t)t * k + j] = exp((double)L[sel[k - 1 - j]] - M) / s;"),
+    # selection bias subtracted instead of added
+    "bias_sign": ("volatile float sum = logits[(size_t)t * E + e] + bias[e];",
+                  "volatile float sum = logits[(size_t)t * E + e] - bias[e];"),
+    # logistic with the wrong sign
+    "sigmoid_sign": ("w[j] = 1.0 / (1.0 + exp(-(double)L[sel[j]]));",
+                     "w[j] = 1.0 / (1.0 + exp((double)L[sel[j]]));"),
+    # ties between equal keys go to the higher index
+    "bias_tie": ("if (best < 0 || key[e] > key[best]) best = e;",
+                 "if (best < 0 || key[e] >= key[best]) best = e;"),
     # histogram off by one in the prefix sum
     "prefix": ("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
 }
@@ -74,6 +92,11 @@ def test_pins_catch_mutation(tmp_path, oracle_mod, name):
             *[(lambda s=s: pins.test_topk_matches_full_sort(o, s)) for s in range(6)],
             lambda: pins.test_topk_special_cases(o),
             lambda: pins.test_gate_weight_two_experts_is_logistic(o),
+            lambda: pins.test_renorm_gates_closed_forms(o),
+            lambda: pins.test_renorm_gates_ignore_unchosen_logits(o),
+            lambda: pins.test_biased_selection_brute_force(o),
+            lambda: pins.test_biased_selection_forces_the_biased_experts(o),
+            lambda: pins.test_gates_at_closed_forms(o),
             *[(lambda s=s: pins.test_histogram_and_permutation_brute_force(o, s)) for s in range(4)],
             lambda: pins.test_gather_is_fancy_index(o),
             lambda: pins.test_gemm_single_expert_is_plain_matmul(o),

@@ -123,6 +123,108 @@ def test_gate_weight_two_experts_is_logistic(oracle_mod):
         assert w[t, 0] == pytest.approx(1.0 / (1.0 + math.exp(-diff)), abs=1e-15)
 
 
+def test_renorm_gates_closed_forms(oracle_mod):
+    """Gates renormalised over the k picks (Mixtral-style): k = 1 gives exactly 1;
+    k = 2 gives the logistic of the two chosen logits' difference; k = E gives the
+    softmax over all experts."""
+    rng = np.random.default_rng(21)
+    L = rng.standard_normal((40, 9)).astype(np.float32) * 3
+    idx, _ = oracle_mod.topk(L, 1)
+    assert np.all(oracle_mod.renorm_gates(L, idx) == 1.0)
+    idx, _ = oracle_mod.topk(L, 2)
+    w = oracle_mod.renorm_gates(L, idx)
+    for t in range(L.shape[0]):
+        a, b = float(L[t, idx[t, 0]]), float(L[t, idx[t, 1]])
+        assert w[t, 0] == pytest.approx(1.0 / (1.0 + math.exp(b - a)), abs=1e-15)
+        assert w[t, 1] == pytest.approx(1.0 / (1.0 + math.exp(a - b)), abs=1e-15)
+    idx, w_all = oracle_mod.topk(L, 9)
+    e = np.exp(L.astype(np.float64) - L.max(axis=1, keepdims=True))
+    full = e / e.sum(axis=1, keepdims=True)
+    assert np.allclose(oracle_mod.renorm_gates(L, idx), np.take_along_axis(full, idx, axis=1),
+                       rtol=0, atol=1e-15)
+
+
+def test_renorm_gates_ignore_unchosen_logits(oracle_mod):
+    """Renormalised gates depend only on the chosen logits: lowering the rest
+    changes neither the picks nor the gates, and every token's gates sum to 1
+    with ratios exp(L_j - L_0)."""
+    rng = np.random.default_rng(22)
+    T, E, k = 60, 32, 4
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    idx, _ = oracle_mod.topk(L, k)
+    w = oracle_mod.renorm_gates(L, idx)
+    L2 = L.copy()
+    mask = np.ones_like(L, bool)
+    np.put_along_axis(mask, idx, False, axis=1)
+    L2[mask] -= 5.0
+    idx2, _ = oracle_mod.topk(L2, k)
+    assert np.array_equal(idx, idx2)
+    assert np.array_equal(oracle_mod.renorm_gates(L2, idx2), w)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    lo = np.take_along_axis(L, idx, axis=1).astype(np.float64)
+    assert np.allclose(w / w[:, :1], np.exp(lo - lo[:, :1]), rtol=1e-14, atol=0)
+
+
+def test_biased_selection_brute_force(oracle_mod):
+    """Selection on fp32(logit + bias): zero bias gives the plain top-k; on tiny
+    inputs with many ties the picks equal a stable sort of the keys (numpy's
+    fp32 addition, largest key first, lower index first between equals)."""
+    rng = np.random.default_rng(23)
+    for trial in range(30):
+        T, E = int(rng.integers(1, 20)), int(rng.integers(1, 12))
+        k = int(rng.integers(1, E + 1))
+        L = _random_logits(rng, T, E, coarse=True)
+        assert np.array_equal(oracle_mod.select_biased(L, np.zeros(E, np.float32), k),
+                              oracle_mod.topk(L, k)[0])
+        b = (np.round(rng.standard_normal(E) * 2) / 2).astype(np.float32)
+        idx = oracle_mod.select_biased(L, b, k)
+        key = L + b[None, :]
+        assert key.dtype == np.float32
+        for t in range(T):
+            order = np.lexsort((np.arange(E), -key[t].astype(np.float64)))
+            assert idx[t].tolist() == order[:k].tolist(), (trial, t)
+
+
+def test_biased_selection_forces_the_biased_experts(oracle_mod):
+    """A bias far above the logits' spread makes the biased experts the picks,
+    ordered among themselves by logit; the gates ignore the bias."""
+    rng = np.random.default_rng(24)
+    T, E, k = 50, 16, 3
+    L = _random_logits(rng, T, E, coarse=True)
+    hot = np.array([13, 2, 7])
+    b = np.zeros(E, np.float32)
+    b[hot] = 512.0
+    idx = oracle_mod.select_biased(L, b, k)
+    for t in range(T):
+        want = sorted(hot.tolist(), key=lambda e: (-float(L[t, e]), e))
+        assert idx[t].tolist() == want
+    w = oracle_mod.gates_at(L, idx)
+    e = np.exp(L.astype(np.float64) - L.max(axis=1, keepdims=True))
+    assert np.allclose(w, np.take_along_axis(e / e.sum(axis=1, keepdims=True), idx, axis=1),
+                       rtol=0, atol=1e-15)
+
+
+def test_gates_at_closed_forms(oracle_mod):
+    """Logistic gates: 1/2 at 0 and (1 + tanh(x/2)) / 2 elsewhere; renormalised,
+    a single pick gets exactly 1 and k picks sum to 1; softmax gates at the
+    plain top-k picks equal oracle_topk's own weights."""
+    rng = np.random.default_rng(25)
+    L = (rng.standard_normal((30, 12)) * 3).astype(np.float32)
+    L[0, :] = 0.0
+    idx, w_soft = oracle_mod.topk(L, 4)
+    w = oracle_mod.gates_at(L, idx, sigmoid=True)
+    assert np.all(w[0] == 0.5)
+    x = np.take_along_axis(L, idx, axis=1).astype(np.float64)
+    assert np.allclose(w, (1.0 + np.tanh(x / 2)) / 2, rtol=0, atol=1e-15)
+    wr = oracle_mod.gates_at(L, idx, sigmoid=True, renorm=True)
+    assert np.allclose(wr.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    assert np.allclose(wr * w.sum(axis=1, keepdims=True), w, rtol=1e-14, atol=0)
+    assert np.all(oracle_mod.gates_at(L, idx[:, :1], sigmoid=True, renorm=True) == 1.0)
+    assert np.allclose(oracle_mod.gates_at(L, idx), w_soft, rtol=0, atol=1e-16)
+    assert np.allclose(oracle_mod.gates_at(L, idx, renorm=True), oracle_mod.renorm_gates(L, idx),
+                       rtol=0, atol=1e-15)
+
+
 def test_topk_rejects_nan(oracle_mod):
     L = np.array([[0.0, np.nan, 1.0]], np.float32)
     with pytest.raises(ValueError):

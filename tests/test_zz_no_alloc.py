@@ -34,11 +34,12 @@ def _args(o):
     return (o["topk_idx"], o["topk_w"], o["counts"], o["offsets"], o["perm"], o["dest"])
 
 
-@pytest.mark.parametrize("name", ["finegrained", "deepseek_v3"])
-def test_noalloc_route_matches_workspace_route_twice(name):
+@pytest.mark.parametrize("name,route_flags", [("finegrained", 0), ("deepseek_v3", 0),
+                                              ("mixtral", binding.MOE_ROUTE_RENORM)])
+def test_noalloc_route_matches_workspace_route_twice(name, route_flags):
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = workloads.WORKLOADS[name]
-    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, route_flags=route_flags)
     ws = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
     for call, seed in enumerate((11, 12)):
         logits = workloads.make_inputs(wl, seed=seed, with_weights=False)["logits"].to(dev)
