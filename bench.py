@@ -388,7 +388,8 @@ def run_ours(args, wl):
                 "unit": "GB/s", "peak_source": f"{peak_src} (copy bandwidth)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = _traffic_per_launch(wl.name)
-    roof["kernel"] = "dispatch_gemm_kernel"
+    roof["kernel"] = ("dispatch_gemm_pair_kernel (CTA pairs, 256-row tiles)"
+                      if plan.info["tile_m"] == 256 else "dispatch_gemm_kernel (128-row tiles)")
     roof["algorithmic_flops"] = flops
     roof["algorithmic_bytes"] = alg_bytes
     line = {
@@ -397,7 +398,8 @@ def run_ours(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**wl.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "tile_n": plan.info["tile_n"], "producer_ctas": plan.info["producer_ctas"],
+                   "tile_m": plan.info["tile_m"], "tile_n": plan.info["tile_n"],
+                   "producer_ctas": plan.info["producer_ctas"],
                    "num_ctas": plan.info["num_ctas"], "stages": plan.info["stages"]},
         "tokens_per_s": world * K * wl.T / total_s,
         "pct_bf16_peak": 100.0 * value / world / tf_peak,
