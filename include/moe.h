@@ -210,6 +210,45 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
                                void* workspace, int32_t* dev_status, void* stream);
 
 /*
+ * moe_dispatch_gemm_swiglu -- moe_dispatch_gemm for a gated (SwiGLU) expert
+ * up-projection.  The plan's N is 2F: W1's first F columns are the gate
+ * projection and the last F the up projection.  Each GEMM tile computes the
+ * gate and the up columns of the same F-columns side by side (tile_n/2 of
+ * each) and its epilogue writes
+ *   H[i][f] = bf16( silu(g) * u ),  g = (A_i . W1[e][:, f]),
+ *                                  u = (A_i . W1[e][:, F+f]),  silu(g) = g / (1 + e^-g)
+ * with g, u accumulated in fp32 and the activation in fp32, rounded once to
+ * bf16 (nearest even).  The articles fix no expert activation; this entry
+ * point serves Mixtral- and DeepSeek-style experts, whose down projection is
+ * moe_grouped_gemm on H.
+ *   W1  in:  bf16 [E][d][2F] (2F = the plan's N; F a multiple of 8).
+ *   H   out: bf16 [S][F], destination order, 16-byte aligned.
+ * Other arguments as for moe_dispatch_gemm.  MOE_ERR_UNSUPPORTED for a plan
+ * made with tile_n = 192 (the halves must be whole 64-column boxes).
+ */
+MOE_API moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x,
+                                      const int32_t* offsets, const int32_t* perm,
+                                      const uint16_t* W1, void* const* recv, uint16_t* H,
+                                      void* workspace, int32_t* dev_status, void* stream);
+
+/*
+ * moe_grouped_gemm -- the per-expert grouped GEMM alone, on rows the caller
+ * has already laid out in destination order (for example H from
+ * moe_dispatch_gemm_swiglu, for the down projection).  Same kernel and tiles
+ * as moe_dispatch_gemm with no scatter role and no ready flags.
+ *   A        in:  bf16 [S][d] (the plan's d), destination order, 16-byte aligned.
+ *   offsets  in:  int32 [E+1]: expert e owns rows [offsets[e], offsets[e+1]);
+ *                 offsets[E] must equal S = T*k.
+ *   W        in:  bf16 [E][d][N].
+ *   Y        out: fp32 [S][N]; Y[i] = A[i] x W[e(i)].
+ * Workspace and status as for moe_dispatch_gemm (the plan's workspace; a plan
+ * may serve both entry points on one stream).  Launches one kernel.
+ */
+MOE_API moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const int32_t* offsets,
+                                      const uint16_t* W, float* Y, void* workspace,
+                                      int32_t* dev_status, void* stream);
+
+/*
  * moe_router_logits -- the step before the path: the router logits that
  * moe_route consumes, L = x @ W_r + bias, on the GPU.  The articles name no
  * router; this library fixes its arithmetic so that routing stays bit-exact

@@ -64,7 +64,8 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
             "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
-            "moe_router_logits", "moe_route_biased")
+            "moe_router_logits", "moe_route_biased", "moe_dispatch_gemm_swiglu",
+            "moe_grouped_gemm")
 
 
 def load_library(path: str = LIB_PATH):
@@ -90,6 +91,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_biased.restype = I32
     lib.moe_dispatch_gemm.argtypes = [VP] * 10
     lib.moe_dispatch_gemm.restype = I32
+    lib.moe_dispatch_gemm_swiglu.argtypes = [VP] * 10
+    lib.moe_dispatch_gemm_swiglu.restype = I32
+    lib.moe_grouped_gemm.argtypes = [VP] * 8
+    lib.moe_grouped_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
     lib.moe_router_logits.argtypes = [VP] * 6
@@ -196,6 +201,25 @@ def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, worksp
     _check(rc, "moe_dispatch_gemm")
 
 
+def moe_dispatch_gemm_swiglu(plan: Plan, x, offsets, perm, W1, recv: Sequence, H, workspace,
+                             dev_status, stream=None) -> None:
+    """Fused dispatch + gated up-projection: H = silu(x W1_gate) * (x W1_up), bf16."""
+    arr = (ctypes.c_void_p * max(1, len(recv)))(*[_ptr(r) for r in recv])
+    rc = load_library().moe_dispatch_gemm_swiglu(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm),
+                                                 _ptr(W1), ctypes.cast(arr, ctypes.c_void_p),
+                                                 _ptr(H), _ptr(workspace), _ptr(dev_status),
+                                                 _stream(stream, plan.device))
+    _check(rc, "moe_dispatch_gemm_swiglu")
+
+
+def moe_grouped_gemm(plan: Plan, A, offsets, W, Y, workspace, dev_status, stream=None) -> None:
+    """Per-expert grouped GEMM on rows already in destination order (no scatter)."""
+    rc = load_library().moe_grouped_gemm(plan.handle, _ptr(A), _ptr(offsets), _ptr(W), _ptr(Y),
+                                         _ptr(workspace), _ptr(dev_status),
+                                         _stream(stream, plan.device))
+    _check(rc, "moe_grouped_gemm")
+
+
 def moe_router_logits(plan: Plan, x, W_r, bias, logits, stream=None) -> None:
     rc = load_library().moe_router_logits(plan.handle, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(logits),
                                           _stream(stream, plan.device))
@@ -216,9 +240,11 @@ def moe_read_status(dev_status, stream=None) -> tuple[int, list[int]]:
 
 class MoeBuffers:
     """Device buffers of one layer shape, allocated with PyTorch (the caller's
-    side of the ABI): routing outputs, R receive buffers, Y, workspace, status."""
+    side of the ABI): routing outputs, R receive buffers, the GEMM output, workspace,
+    status.  out="Y": fp32 Y [S][N] (moe_dispatch_gemm); out="H": bf16 H [S][N/2]
+    (moe_dispatch_gemm_swiglu)."""
 
-    def __init__(self, plan: Plan, device="cuda"):
+    def __init__(self, plan: Plan, device="cuda", out: str = "Y"):
         s = plan.shape
         S = s.T * s.k
         R = s.num_ranks or 1
@@ -232,7 +258,8 @@ class MoeBuffers:
         self.perm = torch.empty(S, **i32)
         self.dest = torch.empty(S, **i32)
         self.recv = [torch.empty(max(cap, 1), s.d, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-        self.Y = torch.empty(S, s.N, dtype=torch.float32, device=dev)
+        self.Y = torch.empty(S, s.N, dtype=torch.float32, device=dev) if out == "Y" else None
+        self.H = torch.empty(S, s.N // 2, dtype=torch.bfloat16, device=dev) if out == "H" else None
         self.workspace = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
         self.status = torch.zeros(4, **i32)
 
@@ -245,6 +272,11 @@ def route(plan: Plan, logits, bufs: MoeBuffers, stream=None, selection_bias=None
 def dispatch_gemm(plan: Plan, x, W, bufs: MoeBuffers, stream=None):
     moe_dispatch_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.recv, bufs.Y, bufs.workspace,
                       bufs.status, stream)
+
+
+def dispatch_gemm_swiglu(plan: Plan, x, W1, bufs: MoeBuffers, stream=None):
+    moe_dispatch_gemm_swiglu(plan, x, bufs.offsets, bufs.perm, W1, bufs.recv, bufs.H,
+                             bufs.workspace, bufs.status, stream)
 
 
 def forward(plan: Plan, logits, x, W, bufs: MoeBuffers, stream=None):

@@ -34,6 +34,8 @@
 //    MOE_ERR_DEVICE and all roles leave through the same teardown (drain of
 //    issued TMA loads and MMAs, TMEM release).  The last CTA to finish resets
 //    the workspace counters and records the epoch.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -396,6 +398,88 @@ __device__ __forceinline__ void store_block_rows(float* tile, const uint32_t (&v
     __syncwarp();
 }
 
+// Gated (SwiGLU) epilogue of one 32-column block: h = silu(g) * u with
+// silu(g) = g / (1 + e^-g), fp32, rounded once to bf16 (nearest even).  Each lane
+// holds one row; the row's 64 bytes go through the same padded shared-memory tile,
+// so every store instruction writes 8 rows x 64 B.  With the stride of 36 words the
+// 8 lanes of each 16-byte access phase hit distinct banks, writing and reading.
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+__device__ __forceinline__ void store_block_rows_glu(float* tile_f, const uint32_t (&g)[32],
+                                                     const uint32_t (&u)[32], uint16_t* hbase,
+                                                     size_t ld, int rows_valid, int cols_valid,
+                                                     int lane) {
+    uint32_t* tile = reinterpret_cast<uint32_t*>(tile_f);
+    uint4* mine = reinterpret_cast<uint4*>(tile + lane * kEpiStride);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = 8 * k + 2 * i;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(
+                swiglu(__uint_as_float(g[c]), __uint_as_float(u[c])),
+                swiglu(__uint_as_float(g[c + 1]), __uint_as_float(u[c + 1])));  // .x = column c
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        mine[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+    const int sub = lane & 7;     // row within a group of 8
+    const int chunk = lane >> 3;  // 8-column chunk of the 32
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int row = 8 * j + sub;
+        if (row < rows_valid && 8 * chunk < cols_valid)
+            *reinterpret_cast<uint4*>(hbase + (size_t)row * ld + 8 * chunk) =
+                *reinterpret_cast<const uint4*>(tile + row * kEpiStride + 4 * chunk);
+    }
+    __syncwarp();
+}
+
+// Epilogue of one accumulator (single or pair tile, `bn` columns) for one warp's
+// 32-row lane quarter: Y in fp32, or in gated mode H = silu(gate) * up in bf16 from
+// the gate columns [0, bn/2) and the up columns [bn/2, bn).
+__device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const TileInfo& ti, int bn,
+                                              uint32_t tbase, int q, int lane, float* epi) {
+    const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
+    if (p.glu) {
+        const int half = bn / 2;
+        const int fcols = min(half, p.F - ti.n * half);
+        uint16_t* hbase = p.H + (size_t)(ti.row0 + 32 * q) * p.F + (size_t)ti.n * half;
+        for (int c = 0; c < fcols; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32(tbase + (uint32_t)c, g);
+            tmem_ld_32x32(tbase + (uint32_t)(half + c), u);
+            tmem_ld_wait(g);
+            tmem_ld_wait(u);
+            if (rows_valid > 0)
+                store_block_rows_glu(epi, g, u, hbase + c, (size_t)p.F, rows_valid, fcols - c, lane);
+        }
+    } else {
+        float* ybase = p.Y + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
+        const int ncols = min(bn, p.N - ti.n * bn);
+        for (int c = 0; c < ncols; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32(tbase + (uint32_t)c, v);
+            tmem_ld_wait(v);
+            if (rows_valid > 0) store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
+        }
+    }
+}
+
+// First column in W of the 64-column B box `j` of a tile whose columns start at
+// `ncol` (plain) or, in gated mode, whose gate and up halves each hold `half`
+// columns starting at F-column n * half: boxes [0, half/64) are gate columns,
+// the rest the matching up columns F + ...
+__device__ __forceinline__ int b_box_col(const DispatchGemmParams& p, int n, int bn, int j) {
+    if (!p.glu) return n * bn + 64 * j;
+    const int half = bn / 2;
+    const int hb = half / 64;
+    const int up = j >= hb ? 1 : 0;
+    return up * p.F + n * half + 64 * (j - up * hb);
+}
+
 template <int BN, int STAGES>
 struct Cfg {
     static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB
@@ -472,7 +556,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             slot = 0;
             sphase ^= 1u;
         }
-        flag = ti.rows > 0 ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        flag = (ti.rows > 0 && !p.a_ready) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
         return true;
     };
 
@@ -484,7 +568,6 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
-        const int ncol = cur.n * BN;
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -503,7 +586,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
-                            ncol + 64 * j, brow + kb * kTileK);
+                            b_box_col(p, cur.n, BN, j), brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -598,16 +681,8 @@ __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 9);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
-        const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
-        float* ybase = p.Y + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * BN;
-        const int ncols = min(BN, p.N - ti.n * BN);
         const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(32 * q) << 16);
-        for (int c = 0; c < ncols; c += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32(tbase + (uint32_t)c, v);
-            tmem_ld_wait(v);
-            if (rows_valid > 0) store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
-        }
+        epilogue_tile(p, ti, BN, tbase, q, lane, epi);
         tc_fence_before();
         mbar_arrive(smem_addr(&ctl->tempty[acc]));
         acc ^= 1;
@@ -831,7 +906,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             slot = 0;
             sphase ^= 1u;
         }
-        flag = (ti.e >= 0 && ti.rows > 0) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        flag = (ti.e >= 0 && ti.rows > 0 && !p.a_ready) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
         got = true;
         return true;
     };
@@ -845,7 +920,8 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
-        const int ncol = cur.n * C::kBN + (leader ? 0 : 128);
+        // this CTA's 128 of the pair tile's 256 B columns: boxes 0-1 (leader) or 2-3
+        const int ncol = b_box_col(p, cur.n, C::kBN, leader ? 0 : 2);
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -970,17 +1046,9 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 30, true, true);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
-        const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
-        if (rows_valid > 0) {
-            float* ybase = p.Y + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * C::kBN;
-            const int ncols = min(C::kBN, p.N - ti.n * C::kBN);
+        if (ti.rows - 32 * q > 0) {  // the odd half of a pair tile may hold fewer rows
             const uint32_t tbase = tmem_base + (uint32_t)(acc * C::kBN) + ((uint32_t)(32 * q) << 16);
-            for (int c = 0; c < ncols; c += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32(tbase + (uint32_t)c, v);
-                tmem_ld_wait(v);
-                store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
-            }
+            epilogue_tile(p, ti, C::kBN, tbase, q, lane, epi);
         }
         tc_fence_before();
         __syncwarp();

@@ -33,7 +33,9 @@ struct moe_plan_s {
     std::mutex mu;
     bool maps_valid = false;
     const void* map_W = nullptr;
-    const void* map_recv[kMaxRanks] = {};
+    int map_nA = 0;          // A buffers encoded: R receive buffers, or 1 caller buffer
+    uint64_t map_rows = 0;   // rows of each A buffer
+    const void* map_A[kMaxRanks] = {};
     CUtensorMap a_maps[kMaxRanks];
     CUtensorMap b_map;
 };
@@ -311,50 +313,77 @@ moe_status_t moe_route_biased(moe_plan_t plan, const float* logits, const float*
     return MOE_OK;
 }
 
-moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
-                               const int32_t* perm, const uint16_t* W, void* const* recv, float* Y,
-                               void* workspace, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped };
+
+// The three entry points that run the persistent GEMM kernel.  kDispatch and
+// kDispatchSwiglu scatter x into the receive buffers and compute on the rows
+// as they land; kGrouped computes on rows the caller has already laid out.
+moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const int32_t* offsets,
+                      const int32_t* perm, const uint16_t* W, void* const* recv, const uint16_t* A,
+                      float* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
+    const bool glu = mode == GemmMode::kDispatchSwiglu;
+    if (glu && plan->tile_n == 192) return MOE_ERR_UNSUPPORTED;  // halves must be whole 64-column boxes
     if (plan->T == 0) return MOE_OK;
-    if (!x || !offsets || !perm || !W || !recv || !Y) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(offsets, 4) ||
-        !aligned(perm, 4))
-        return MOE_ERR_INVALID_ARG;
-    for (int r = 0; r < plan->R; ++r)
-        if (!recv[r] || !aligned(recv[r], 16)) return MOE_ERR_INVALID_ARG;
+    if (!offsets || !W || !aligned(W, 16) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
+    if (glu ? (!H || !aligned(H, 16)) : (!Y || !aligned(Y, 16))) return MOE_ERR_INVALID_ARG;
+    const bool grouped = mode == GemmMode::kGrouped;
+    const int nA = grouped ? 1 : plan->R;
+    const void* abuf[kMaxRanks] = {};
+    if (grouped) {
+        if (!A || !aligned(A, 16)) return MOE_ERR_INVALID_ARG;
+        abuf[0] = A;
+    } else {
+        if (!x || !perm || !recv || !aligned(x, 16) || !aligned(perm, 4)) return MOE_ERR_INVALID_ARG;
+        for (int r = 0; r < plan->R; ++r) {
+            if (!recv[r] || !aligned(recv[r], 16)) return MOE_ERR_INVALID_ARG;
+            abuf[r] = recv[r];
+        }
+    }
+    const uint64_t arows = grouped ? (uint64_t)plan->S : (uint64_t)plan->cap;
     DeviceGuard guard(plan->device);
     if (!guard.ok) return MOE_ERR_CUDA;
 
     DispatchGemmParams prm;
     {
         std::lock_guard<std::mutex> lock(plan->mu);
-        bool same = plan->maps_valid && plan->map_W == W;
-        for (int r = 0; same && r < plan->R; ++r) same = plan->map_recv[r] == recv[r];
+        bool same = plan->maps_valid && plan->map_W == W && plan->map_nA == nA && plan->map_rows == arows;
+        for (int r = 0; same && r < nA; ++r) same = plan->map_A[r] == abuf[r];
         if (!same) {
             plan->maps_valid = false;
-            for (int r = 0; r < plan->R; ++r)
-                if (!encode_bf16_2d(&plan->a_maps[r], recv[r], (uint64_t)plan->cap, (uint64_t)plan->d,
-                                    kTileK, kTileM))
+            for (int r = 0; r < nA; ++r)
+                if (!encode_bf16_2d(&plan->a_maps[r], abuf[r], arows, (uint64_t)plan->d, kTileK, kTileM))
                     return MOE_ERR_CUDA;
             if (!encode_bf16_2d(&plan->b_map, W, (uint64_t)plan->E * plan->d, (uint64_t)plan->N, 64,
                                 kTileK))
                 return MOE_ERR_CUDA;
             plan->map_W = W;
-            for (int r = 0; r < plan->R; ++r) plan->map_recv[r] = recv[r];
+            plan->map_nA = nA;
+            plan->map_rows = arows;
+            for (int r = 0; r < nA; ++r) plan->map_A[r] = abuf[r];
             plan->maps_valid = true;
         }
         std::memset(&prm, 0, sizeof prm);
-        for (int r = 0; r < plan->R; ++r) prm.a_map[r] = plan->a_maps[r];
+        for (int r = 0; r < nA; ++r) prm.a_map[r] = plan->a_maps[r];
         prm.b_map = plan->b_map;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.x = x;
     prm.offsets = offsets;
     prm.perm = perm;
-    for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
+    if (!grouped)
+        for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
     prm.Y = Y;
+    prm.H = H;
+    prm.glu = glu ? 1 : 0;
+    prm.F = plan->N / 2;
+    prm.a_ready = grouped ? 1 : 0;
     prm.hdr = reinterpret_cast<uint32_t*>(ws);
     prm.flags = reinterpret_cast<uint32_t*>(ws + plan->ws.flags_off);
     prm.chunk_cnt = reinterpret_cast<uint32_t*>(ws + plan->ws.chunk_cnt_off);
@@ -365,12 +394,14 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
     prm.E = plan->E;
     prm.k = plan->k;
     prm.N = plan->N;
-    prm.R = plan->R;
-    prm.cap = plan->cap;
+    prm.R = grouped ? 1 : plan->R;
+    prm.cap = grouped ? (int)plan->S : plan->cap;
     prm.tile_n = plan->tile_n;
-    prm.n_tiles = (plan->N + plan->tile_n - 1) / plan->tile_n;
+    const int tile_cols = glu ? plan->tile_n / 2 : plan->tile_n;  // output columns per tile
+    const int out_cols = glu ? plan->N / 2 : plan->N;
+    prm.n_tiles = (out_cols + tile_cols - 1) / tile_cols;
     prm.k_blocks = plan->d / kTileK;
-    prm.producer_ctas = plan->producer_ctas;
+    prm.producer_ctas = grouped ? 0 : plan->producer_ctas;
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
@@ -383,6 +414,32 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
         return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                               const int32_t* perm, const uint16_t* W, void* const* recv, float* Y,
+                               void* workspace, int32_t* dev_status, void* stream) {
+    return run_gemm(plan, GemmMode::kDispatch, x, offsets, perm, W, recv, nullptr, Y, nullptr,
+                    workspace, dev_status, stream);
+}
+
+moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                                      const int32_t* perm, const uint16_t* W1, void* const* recv,
+                                      uint16_t* H, void* workspace, int32_t* dev_status,
+                                      void* stream) {
+    return run_gemm(plan, GemmMode::kDispatchSwiglu, x, offsets, perm, W1, recv, nullptr, nullptr, H,
+                    workspace, dev_status, stream);
+}
+
+moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const int32_t* offsets,
+                              const uint16_t* W, float* Y, void* workspace, int32_t* dev_status,
+                              void* stream) {
+    return run_gemm(plan, GemmMode::kGrouped, nullptr, offsets, nullptr, W, nullptr, A, Y, nullptr,
+                    workspace, dev_status, stream);
 }
 
 moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_t* W_r,

@@ -94,6 +94,10 @@ struct DispatchGemmParams {
     int max_mtiles;                 // size of flags[] and chunk_cnt[]
     int skip_publish;               // m-tile whose flag is never published, or -1
     int band;                       // row tiles per schedule band; 0 = the whole expert
+    int glu;                        // 1: W = [gate | up], each F = N/2 wide; out H, not Y
+    int F;                          // N/2 when glu
+    uint16_t* H;                    // glu: bf16 [S][F], silu(gate) * up
+    int a_ready;                    // 1: A rows are already in a_map[0] (no scatter, no flags)
 };
 
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,

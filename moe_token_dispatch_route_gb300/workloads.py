@@ -133,6 +133,36 @@ def make_weights(wl: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
     return W
 
 
+def _normal_bf16(shape, scale: float, seed: int, device) -> torch.Tensor:
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    out = torch.empty(*shape, dtype=torch.bfloat16, device=dev)
+    for e in range(shape[0]):  # one slice at a time: no fp32 copy of the whole tensor
+        out[e] = (torch.randn(*shape[1:], generator=g, device=dev) * scale).to(torch.bfloat16)
+    return out
+
+
+def make_ffn_weights(wl: Workload, F: int, seed: int = 0, device="cpu"):
+    """Gated expert FFN weights, bf16: W1 [E, d, 2F] ~ N(0, 1/d) with the gate
+    projection in columns [0, F) and the up projection in [F, 2F) (seed + 4), and
+    the down projection W2 [E, F, d] ~ N(0, 1/F) (seed + 5)."""
+    W1 = _normal_bf16((wl.E, wl.d, 2 * F), 1.0 / math.sqrt(wl.d), seed + 4, device)
+    W2 = _normal_bf16((wl.E, F, wl.d), 1.0 / math.sqrt(F), seed + 5, device)
+    return W1, W2
+
+
+def make_rows(S: int, width: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Rows already in destination order for the grouped GEMM alone: bf16 [S, width]
+    ~ N(0, 1/4) (the spread of silu(g) * u for g, u ~ N(0, 1)), seed + 6."""
+    dev = torch.device(device)
+    g = _gen(seed + 6, dev)
+    out = torch.empty(S, width, dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, S, 1024):  # blocks of rows: no fp32 copy of the whole tensor
+        r1 = min(S, r0 + 1024)
+        out[r0:r1] = (torch.randn(r1 - r0, width, generator=g, device=dev) * 0.5).to(torch.bfloat16)
+    return out
+
+
 def make_inputs(wl: Workload, seed: int = 0, w_device="cpu", with_weights: bool = True) -> dict:
     """All inputs of one step: x, W_r, bias, logits on the host; W on `w_device`."""
     x = make_x(wl, seed)

@@ -19,4 +19,6 @@ from .oracle import (  # noqa: F401
     route,
     combine,
     router_logits,
+    swiglu,
+    round_bf16,
 )

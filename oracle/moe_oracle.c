@@ -288,6 +288,64 @@ ORACLE_API double oracle_gemm_entry(const uint16_t* row, const uint16_t* We,
 }
 
 /*
+ * Gated expert activation (SwiGLU), applied to the up-projection output of
+ * one destination row: G is [S][2F] with the gate projection in columns
+ * [0, F) and the up projection in [F, 2F);
+ *   H[i][f] = silu(G[i][f]) * G[i][F + f],   silu(g) = g / (1 + exp(-g)),
+ * in fp64.
+ */
+ORACLE_API void oracle_swiglu(const double* G, long S, int F, double* H) {
+    for (long i = 0; i < S; ++i)
+        for (int f = 0; f < F; ++f) {
+            const double g = G[(size_t)i * 2 * F + f];
+            const double u = G[(size_t)i * 2 * F + F + f];
+            H[(size_t)i * F + f] = g / (1.0 + exp(-g)) * u;
+        }
+}
+
+/*
+ * Rounding to bf16, round to nearest with ties to even, from fp64: the bf16
+ * value is the nearest number of the form m * 2^q with |m| < 2^8 (8
+ * significant bits) in bf16's exponent range; between two equally near, the
+ * one with even m.  Values beyond the largest finite bf16 (after rounding)
+ * become infinities; NaN becomes the quiet NaN 0x7FC0.  Subnormal bf16
+ * results (|v| < 2^-126) are rounded on the fixed grid of spacing 2^-133.
+ */
+ORACLE_API void oracle_round_bf16(const double* v, long n, uint16_t* out) {
+    for (long i = 0; i < n; ++i) {
+        const double x = v[i];
+        if (isnan(x)) { out[i] = 0x7FC0; continue; }
+        const uint16_t sign = signbit(x) ? 0x8000 : 0;
+        const double a = fabs(x);
+        if (a == 0.0) { out[i] = sign; continue; }
+        int q;
+        (void)frexp(a, &q);            /* a = f * 2^q, 0.5 <= f < 1 */
+        int e = q - 1;                 /* 2^e <= a < 2^(e+1) */
+        if (e < -126) e = -126;        /* subnormal range: fixed spacing */
+        const double ulp = ldexp(1.0, e - 7);
+        double m = a / ulp;            /* exact: a power-of-two scaling */
+        double r = floor(m);
+        const double frac = m - r;
+        if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+        const double y = r * ulp;      /* may reach 2^(e+1): still exact */
+        if (y == 0.0) { out[i] = sign; continue; }  /* below half the smallest subnormal */
+        if (y > 3.3895313892515355e38) { out[i] = sign | 0x7F80; continue; }  /* above bf16 max */
+        /* encode y: exponent and 7 fraction bits */
+        int qy;
+        const double fy = frexp(y, &qy);
+        int ey = qy - 1;
+        uint16_t bits;
+        if (ey < -126) {
+            bits = (uint16_t)(y / ldexp(1.0, -133));      /* subnormal: m * 2^-133 */
+        } else {
+            const double mant = fy * 2.0 - 1.0;           /* in [0, 1) */
+            bits = (uint16_t)(((ey + 127) << 7) | (int)(mant * 128.0));
+        }
+        out[i] = sign | bits;
+    }
+}
+
+/*
  * Expert that owns destination row `row`: the e with
  * offsets[e] <= row < offsets[e+1] (a linear scan; empty experts are skipped
  * because their segment is empty).

@@ -65,6 +65,10 @@ def _load():
             lib.oracle_router_logits.restype = None
             lib.oracle_combine.argtypes = [P, P, P, I, I, I, P]
             lib.oracle_combine.restype = None
+            lib.oracle_swiglu.argtypes = [P, L, I, P]
+            lib.oracle_swiglu.restype = None
+            lib.oracle_round_bf16.argtypes = [P, L, P]
+            lib.oracle_round_bf16.restype = None
             lib.oracle_expert_of_row.argtypes = [P, I, L]
             lib.oracle_expert_of_row.restype = I
             _lib = lib
@@ -231,6 +235,24 @@ def combine(Y: np.ndarray, topk_w: np.ndarray, dest: np.ndarray):
     assert ds.shape[0] == T * k
     out = np.empty((T, N), np.float64)
     _load().oracle_combine(_p(Yd), _p(w), _p(ds), T, k, N, _p(out))
+    return out
+
+
+def swiglu(G: np.ndarray):
+    """Gated activation of up-projection rows: G [S, 2F] (gate | up) -> H float64 [S, F]."""
+    Gd = np.ascontiguousarray(G, dtype=np.float64)
+    S, F2 = Gd.shape
+    assert F2 % 2 == 0
+    H = np.empty((S, F2 // 2), np.float64)
+    _load().oracle_swiglu(_p(Gd), S, F2 // 2, _p(H))
+    return H
+
+
+def round_bf16(v: np.ndarray):
+    """Round fp64 values to bf16 (nearest, ties to even) -> uint16 bit patterns."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_round_bf16(_p(a), a.size, _p(out))
     return out
 
 

@@ -47,6 +47,12 @@ MUTATIONS = {
     # ties between equal keys go to the higher index
     "bias_tie": ("if (best < 0 || key[e] > key[best]) best = e;",
                  "if (best < 0 || key[e] >= key[best]) best = e;"),
+    # gated activation applied to the up half instead of the gate half
+    "swiglu_swap": ("H[(size_t)i * F + f] = g / (1.0 + exp(-g)) * u;",
+                    "H[(size_t)i * F + f] = u / (1.0 + exp(-u)) * g;"),
+    # bf16 rounding: ties away from zero instead of to even
+    "round_tie": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+                  "if (frac >= 0.5) r += 1.0;"),
     # histogram off by one in the prefix sum
     "prefix": ("offsets[e + 1] = offsets[e] + counts[e];", "offsets[e + 1] = offsets[e] + counts[e] + (e == 0);"),
 }
@@ -97,6 +103,8 @@ def test_pins_catch_mutation(tmp_path, oracle_mod, name):
             lambda: pins.test_biased_selection_brute_force(o),
             lambda: pins.test_biased_selection_forces_the_biased_experts(o),
             lambda: pins.test_gates_at_closed_forms(o),
+            lambda: pins.test_swiglu_closed_forms(o),
+            lambda: pins.test_round_bf16_ties_and_library(o),
             *[(lambda s=s: pins.test_histogram_and_permutation_brute_force(o, s)) for s in range(4)],
             lambda: pins.test_gather_is_fancy_index(o),
             lambda: pins.test_gemm_single_expert_is_plain_matmul(o),

@@ -225,6 +225,45 @@ def test_gates_at_closed_forms(oracle_mod):
                        rtol=0, atol=1e-15)
 
 
+def test_swiglu_closed_forms(oracle_mod):
+    """silu(g) * u: 0 when g = 0 or u = 0; g * u once e^-g is below half an ulp
+    of 1; (1 + tanh(g/2)) / 2 * g * u in general; gate and up halves not
+    interchangeable."""
+    rng = np.random.default_rng(26)
+    S, F = 7, 24
+    G = rng.standard_normal((S, 2 * F)) * 3
+    G[0, :F] = 0.0
+    G[1, F:] = 0.0
+    G[2, :F] = 50.0
+    H = oracle_mod.swiglu(G)
+    assert np.all(H[0] == 0.0) and np.all(H[1] == 0.0)
+    assert np.array_equal(H[2], 50.0 * G[2, F:])
+    g, u = G[:, :F], G[:, F:]
+    ref = (1.0 + np.tanh(g / 2)) / 2 * g * u  # 1 + tanh cancels for g << 0: absolute bound
+    assert np.all(np.abs(H - ref) <= 1e-15 * np.abs(g * u) + 1e-14 * np.abs(ref))
+    h = oracle_mod.swiglu(np.array([[2.0, 3.0]]))[0, 0]
+    assert h == pytest.approx(2.0 / (1.0 + math.exp(-2.0)) * 3.0, rel=1e-15)
+    assert h != pytest.approx(3.0 / (1.0 + math.exp(-3.0)) * 2.0, rel=1e-3)
+
+
+def test_round_bf16_ties_and_library(oracle_mod):
+    """Round to nearest, ties to even: the halfway points around 1 and 3;
+    then fp32-representable values of every magnitude (subnormal, overflow,
+    signed zero) against torch's fp32 -> bf16 conversion, which is the same
+    rounding done once."""
+    torch = pytest.importorskip("torch")
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 3 + 2 ** -7, 3 + 3 * 2 ** -7,
+                     1 + 2 ** -8 + 2 ** -30])
+    want = [0x3F80, 0x3F82, 0xBF80, 0x4040, 0x4042, 0x3F81]
+    assert oracle_mod.round_bf16(ties).tolist() == want
+    rng = np.random.default_rng(27)
+    v32 = (rng.standard_normal(20000) * np.exp(rng.uniform(-95, 86, 20000))).astype(np.float32)
+    v32 = np.concatenate([v32, np.array([0.0, -0.0, 2 ** -133, 2 ** -134, 3 * 2 ** -135, 3.39e38],
+                                        np.float32)])
+    ref = torch.from_numpy(v32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle_mod.round_bf16(v32.astype(np.float64)), ref)
+
+
 def test_topk_rejects_nan(oracle_mod):
     L = np.array([[0.0, np.nan, 1.0]], np.float32)
     with pytest.raises(ValueError):
