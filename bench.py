@@ -48,6 +48,8 @@ def _args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--producer-ctas", type=int, default=0)
+    ap.add_argument("--ffn", choices=["auto", "on", "off"], default="auto",
+                    help="also time the gated (SwiGLU) expert FFN with F = N (auto: Mixtral-shaped only)")
     return ap.parse_args(argv)
 
 
@@ -250,6 +252,67 @@ def run_reference(args, wl):
     return 0
 
 
+def time_swiglu_ffn(wl, inp, x, logits, dev, stream, flush, reps=20):
+    """The whole gated expert FFN of the workload's shape with F = N, timed on its
+    own: route -> fused dispatch + gated up-projection (W1 [E, d, 2F]) -> grouped
+    down projection (W2 [E, F, d]) -> combine.  Per-kernel medians over `reps`
+    steps, L2 flushed between steps."""
+    import torch
+
+    from moe_token_dispatch_route_gb300 import binding, workloads
+
+    F = wl.N
+    W1, W2 = workloads.make_ffn_weights(wl, F, seed=0, device=dev)
+    up = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, 2 * F, num_ranks=wl.R, device=dev.index)
+    bu = binding.MoeBuffers(up, dev, out="H")
+    down = binding.moe_plan(wl.T, F, wl.E, wl.k, wl.d, device=dev.index)
+    ws = torch.zeros(down.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    Y2 = torch.empty(wl.S, wl.d, dtype=torch.float32, device=dev)
+    out = torch.empty(wl.T, wl.d, dtype=torch.float32, device=dev)
+
+    def step(evs=None):
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        binding.route(up, logits, bu, stream)
+        rec(1)
+        binding.dispatch_gemm_swiglu(up, x, W1, bu, stream)
+        rec(2)
+        binding.moe_grouped_gemm(down, bu.H, bu.offsets, W2, Y2, ws, st, stream)
+        rec(3)
+        binding.moe_combine(down, Y2, bu.topk_w, bu.dest, out, stream)
+        rec(4)
+
+    for _ in range(3):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(float(i))
+        step(ev[i])
+    torch.cuda.synchronize(dev)
+    for s_ in (bu.status, st):
+        rc, status = binding.moe_read_status(s_, stream)
+        if rc != 0:
+            raise SystemExit(f"device status in the FFN timing: {status}")
+    med = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(4)]
+    total = statistics.median(e[0].elapsed_time(e[4]) for e in ev)
+    up_flops = 2.0 * wl.S * wl.d * 2 * F
+    down_flops = 2.0 * wl.S * F * wl.d
+    _, tf_peak, peak_src = _peaks()
+    res = {"F": F, "ms": total, "route_ms": med[0], "up_ms": med[1], "down_ms": med[2],
+           "combine_ms": med[3],
+           "up_tflops": up_flops / (med[1] * 1e9), "down_tflops": down_flops / (med[2] * 1e9),
+           "layer_tflops": (up_flops + down_flops) / (total * 1e9),
+           "note": "gated expert FFN with F = N: route -> dispatch + SwiGLU up-projection "
+                   "(bf16 H) -> grouped down projection -> combine; timed separately, not in value"}
+    res["up_frac"] = res["up_tflops"] / tf_peak
+    res["down_frac"] = res["down_tflops"] / tf_peak
+    res["peak_source"] = f"{peak_src} (bf16 burst)"
+    res["tile_m"] = [up.info["tile_m"], down.info["tile_m"]]
+    del W1, W2, bu, Y2, out
+    return res
+
+
 def run_ours(args, wl):
     import torch
 
@@ -342,6 +405,10 @@ def run_ours(args, wl):
     router_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in rev)
     del L_gpu
 
+    ffn = None
+    if args.ffn == "on" or (args.ffn == "auto" and wl.name == "mixtral"):
+        ffn = time_swiglu_ffn(wl, inp, x, logits, dev, stream, flush)
+
     # end to end through the same ABI: pinned host inputs in, Y out, every step
     x_h = inp["x"].pin_memory()
     l_h = inp["logits"].pin_memory()
@@ -420,6 +487,7 @@ def run_ours(args, wl):
                     "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
                     "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,
                     "note": "moe_combine (step after the path), timed separately; not in value"},
+        "swiglu_ffn": ffn,
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step(wl) * K,
