@@ -405,6 +405,22 @@ def run_ours(args, wl):
     router_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in rev)
     del L_gpu
 
+    # the direct-gather variant of the fused kernel (no receive buffers), timed on its own
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for _ in range(3):
+        binding.gather_gemm(plan, x, W, bufs, stream)
+    for a_, b_ in gev:
+        flush.fill_(1.0)
+        a_.record(stream)
+        binding.gather_gemm(plan, x, W, bufs, stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"device status after the gather timing: {st}")
+    gather_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in gev)
+    binding.dispatch_gemm(plan, x, W, bufs, stream)  # leave Y as the path computes it
+
     ffn = None
     if args.ffn == "on" or (args.ffn == "auto" and wl.name == "mixtral"):
         ffn = time_swiglu_ffn(wl, inp, x, logits, dev, stream, flush)
@@ -487,6 +503,12 @@ def run_ours(args, wl):
                     "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
                     "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,
                     "note": "moe_combine (step after the path), timed separately; not in value"},
+        "direct_gather": {"ms": gather_ms, "tflops": flops / (gather_ms * 1e9),
+                          "dispatch_gemm_ms": statistics.median(dg_ms),
+                          "speedup_vs_dispatch": statistics.median(dg_ms) / gather_ms,
+                          "note": "moe_gather_gemm: A rows copied from x by perm straight into the "
+                                  "GEMM's shared memory, no receive buffers (single-CTA kernel); "
+                                  "20 launches, L2 flushed; not in value"},
         "swiglu_ffn": ffn,
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

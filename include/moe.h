@@ -232,6 +232,22 @@ MOE_API moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x
                                       void* workspace, int32_t* dev_status, void* stream);
 
 /*
+ * moe_gather_gemm -- the per-expert grouped GEMM with its A rows gathered
+ * straight from the token rows: for each destination row i, row x[perm[i] / k]
+ * is copied from global memory into the GEMM's shared-memory tile, with no
+ * receive buffer in between (a variant of moe_dispatch_gemm for one GPU, where
+ * the all-to-all has no wire to cross; it measures what landing the rows in a
+ * receive buffer costs).  Y is bit for bit the Y of moe_dispatch_gemm on a
+ * plan with the same tile shape.  CTA-pair plans run it in the single-CTA
+ * kernel with 256-wide tiles.
+ *   x, offsets, perm, W, Y, workspace, dev_status, stream: as for
+ *   moe_dispatch_gemm.  No receive buffers.  Launches one kernel.
+ */
+MOE_API moe_status_t moe_gather_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                                     const int32_t* perm, const uint16_t* W, float* Y,
+                                     void* workspace, int32_t* dev_status, void* stream);
+
+/*
  * moe_grouped_gemm -- the per-expert grouped GEMM alone, on rows the caller
  * has already laid out in destination order (for example H from
  * moe_dispatch_gemm_swiglu, for the down projection).  Same kernel and tiles

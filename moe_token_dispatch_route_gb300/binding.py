@@ -65,7 +65,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
             "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
             "moe_router_logits", "moe_route_biased", "moe_dispatch_gemm_swiglu",
-            "moe_grouped_gemm")
+            "moe_grouped_gemm", "moe_gather_gemm")
 
 
 def load_library(path: str = LIB_PATH):
@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm_swiglu.argtypes = [VP] * 10
     lib.moe_dispatch_gemm_swiglu.restype = I32
     lib.moe_grouped_gemm.argtypes = [VP] * 8
+    lib.moe_gather_gemm.argtypes = [VP] * 9
+    lib.moe_gather_gemm.restype = I32
     lib.moe_grouped_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
@@ -218,6 +220,18 @@ def moe_grouped_gemm(plan: Plan, A, offsets, W, Y, workspace, dev_status, stream
                                          _ptr(workspace), _ptr(dev_status),
                                          _stream(stream, plan.device))
     _check(rc, "moe_grouped_gemm")
+
+
+def moe_gather_gemm(plan: Plan, x, offsets, perm, W, Y, workspace, dev_status, stream=None) -> None:
+    """Grouped GEMM whose A rows are gathered from x by perm (no receive buffers)."""
+    rc = load_library().moe_gather_gemm(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm), _ptr(W),
+                                        _ptr(Y), _ptr(workspace), _ptr(dev_status),
+                                        _stream(stream, plan.device))
+    _check(rc, "moe_gather_gemm")
+
+
+def gather_gemm(plan: Plan, x, W, bufs: "MoeBuffers", stream=None):
+    moe_gather_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.Y, bufs.workspace, bufs.status, stream)
 
 
 def moe_router_logits(plan: Plan, x, W_r, bias, logits, stream=None) -> None:

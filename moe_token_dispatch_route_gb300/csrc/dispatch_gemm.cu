@@ -490,6 +490,7 @@ struct Cfg {
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
+    static_assert(kSmem <= 232448, "more than 227 KB of shared memory per CTA");
     static_assert(BN == 128 || BN == 192 || BN == 256, "tile_n");
     // the scatter stages rows in the stage area: 8 warps x 32 lanes x slots x 16 B
     static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
@@ -511,7 +512,8 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     const uint32_t total_tiles = (uint32_t)mt_base[p.E] * (uint32_t)p.n_tiles;
     const int e_per_rank = p.E / p.R;
     tma_prefetch_map(&p.b_map);
-    for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
+    if (!p.gather)  // no A tensor map in the gather mode
+        for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
     int stage = 0;
     uint32_t phase = 0;
     int slot = 0;
@@ -556,7 +558,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             slot = 0;
             sphase ^= 1u;
         }
-        flag = (ti.rows > 0 && !p.a_ready) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        flag = (ti.rows > 0 && !p.a_ready && !p.gather) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
         return true;
     };
 
@@ -581,8 +583,12 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
                 break;
             }
             const uint32_t fb = smem_addr(&ctl->full[stage]);
-            mbar_arrive_expect_tx(fb, C::kStageBytes);
-            tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
+            if (p.gather) {  // the gather warps fill A and arrive on the same barrier
+                mbar_arrive_expect_tx(fb, C::kBBytes);
+            } else {
+                mbar_arrive_expect_tx(fb, C::kStageBytes);
+                tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
+            }
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
@@ -690,6 +696,111 @@ __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_
     }
 }
 
+// Direct-gather A loads (gather mode, warps 2 and 3): for every tile the warps
+// take from the schedule ring, warp `part` copies the tile's rows
+// [64 part, 64 part + 64) straight from their token rows of x (perm[row] / k)
+// into the stage's A buffer with 16-byte cp.async, in the 128-byte-swizzled
+// K-major layout the MMA descriptors expect (16-byte chunk c of row r lands at
+// r*128 + (c ^ (r%8))*16).  Eight lanes cover one row's 128 bytes of a k-block,
+// so each copy instruction moves four whole 128-byte lines.  Rows past the
+// tile's valid rows are zero-filled.  Each warp keeps up to STAGES-2 stages of
+// copies in flight; once a stage's copies are complete it fences them for the
+// async proxy (the tensor cores read shared memory there) and arrives on the
+// stage's full barrier, which also waits for the other warp and the TMA
+// thread's B bytes.  No receive buffer is written and no ready flag is read.
+// The copies are plain 16-byte cp.async rather than TMA: a TMA copy per
+// gathered row (or tile::gather4) would write single rows into the middle of
+// the 1024-byte swizzle atom, a placement this kernel does not rely on.
+constexpr int kGatherWarp0 = 2;
+constexpr int kGatherWarps = 2;
+constexpr int kGatherRows = kTileM / kGatherWarps;  // rows per warp
+template <int STAGES>
+__device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, const Waiter& w,
+                              int part) {
+    constexpr int kABytes = kTileM * kTileK * 2;  // 128 rows x 64 columns
+    constexpr int kLag = STAGES - 2 >= 1 ? STAGES - 2 : 1;  // stages in flight before an arrive
+    constexpr int kIters = kGatherRows / 4;
+    const int lane = threadIdx.x & 31;
+    const char* xb = reinterpret_cast<const char*>(p.x);
+    const size_t row_bytes = (size_t)p.d * 2;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    int pend[kMaxStages] = {};  // stages whose copies are in flight, oldest first
+    int head = 0, npend = 0;
+    auto retire_oldest = [&](int keep) {
+        cp_async_wait_dyn(keep);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->full[pend[head]]));
+        head = head + 1 == kMaxStages ? 0 : head + 1;
+        --npend;
+    };
+    bool ok = true;
+    while (ok) {
+        const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 40);
+        if (!__all_sync(kFull, got)) break;
+        const TileInfo ti = ctl->ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.rows < 0) break;
+        // this lane copies chunk c of the warp's rows 4i + lane/8 (i < 16): their
+        // token rows, gathered from the lanes that read perm, stay in registers
+        const int c = lane & 7;
+        const int r0 = part * kGatherRows;
+        int tok[kIters];  // -1: past the tile's valid rows
+        {
+            int mine[kGatherRows / 32];
+#pragma unroll
+            for (int j = 0; j < kGatherRows / 32; ++j) {
+                const int r = r0 + lane + 32 * j;
+                mine[j] = r < ti.rows ? __ldg(p.perm + ti.row0 + r) / p.k : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+                // warp row 4i + lane/8 is held by lane (4i + lane/8) % 32 in mine[i / 8]
+                const int src_lane = (4 * i + (lane >> 3)) & 31;
+                tok[i] = __shfl_sync(kFull, mine[i / 8], src_lane);
+            }
+        }
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            bool free_ok = true;
+            if (lane == 0) free_ok = wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 41);
+            if (!__shfl_sync(kFull, free_ok ? 1 : 0, 0)) {
+                ok = false;
+                break;
+            }
+            const uint32_t a0 = smem_addr(sA + stage * kABytes);
+            const size_t kofs = (size_t)kb * (kTileK * 2) + 16 * c;
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+                const int r = r0 + 4 * i + (lane >> 3);
+                const int t = tok[i];
+                cp_async16_cg_zfill(a0 + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4),
+                                    xb + (size_t)(t < 0 ? 0 : t) * row_bytes + kofs, t < 0 ? 0 : 16);
+            }
+            cp_async_commit();
+            int tail = head + npend;
+            if (tail >= kMaxStages) tail -= kMaxStages;
+            pend[tail] = stage;
+            ++npend;
+            if (npend > kLag) retire_oldest(kLag);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // every copy lands and is published before the CTA can leave (also on abort,
+    // so that the TMA thread's drain of the full barriers ends)
+    while (npend > 0) retire_oldest(0);
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     dispatch_gemm_kernel(const __grid_constant__ DispatchGemmParams p) {
@@ -707,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + kGatherWarps : 1);  // + gather warps
             mbar_init(smem_addr(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -716,7 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(smem_addr(&ctl->sfull[r]), 1);
-            mbar_init(smem_addr(&ctl->sempty[r]), 1 + 4);  // MMA thread + 4 epilogue warps
+            // MMA thread + 4 epilogue warps (+ the gather warps)
+            mbar_init(smem_addr(&ctl->sempty[r]), 1 + 4 + (p.gather ? kGatherWarps : 0));
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -763,6 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) mma_role<BN, STAGES>(p, ctl, sA, sB, tmem_base, w);
         __syncwarp();
+    } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
+        gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0);
     } else if (warp >= kEpiWarp0) {
         epilogue_role<BN, STAGES>(p, ctl, tmem_base, w, epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
     }
@@ -821,6 +935,7 @@ struct PairCfg {
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
+    static_assert(kSmem <= 232448, "more than 227 KB of shared memory per CTA");
     static constexpr int kScatterSlots = scatter_slots_per_lane((size_t)STAGES * kStageBytes);
     static_assert(kScatterSlots >= 32, "stage area too small for the scatter staging (two pieces per warp)");
     static_assert((size_t)kScatterSlots * 16 * 32 * (kThreads / 32) <= (size_t)STAGES * kStageBytes,

@@ -29,6 +29,7 @@ struct moe_plan_s {
     int skip_publish = -1;
     int band = 0;
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
+    bool single_ready = false;  // pair plans: single-CTA kernel attributes set (direct gather)
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
     bool maps_valid = false;
@@ -317,7 +318,7 @@ moe_status_t moe_route_biased(moe_plan_t plan, const float* logits, const float*
 
 namespace {
 
-enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped };
+enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped, kGather };
 
 // The three entry points that run the persistent GEMM kernel.  kDispatch and
 // kDispatchSwiglu scatter x into the receive buffers and compute on the rows
@@ -334,11 +335,14 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     if (!offsets || !W || !aligned(W, 16) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
     if (glu ? (!H || !aligned(H, 16)) : (!Y || !aligned(Y, 16))) return MOE_ERR_INVALID_ARG;
     const bool grouped = mode == GemmMode::kGrouped;
-    const int nA = grouped ? 1 : plan->R;
+    const bool gather = mode == GemmMode::kGather;
+    const int nA = grouped ? 1 : gather ? 0 : plan->R;  // A tensor maps (the gather has none)
     const void* abuf[kMaxRanks] = {};
     if (grouped) {
         if (!A || !aligned(A, 16)) return MOE_ERR_INVALID_ARG;
         abuf[0] = A;
+    } else if (gather) {
+        if (!x || !perm || !aligned(x, 16) || !aligned(perm, 4)) return MOE_ERR_INVALID_ARG;
     } else {
         if (!x || !perm || !recv || !aligned(x, 16) || !aligned(perm, 4)) return MOE_ERR_INVALID_ARG;
         for (int r = 0; r < plan->R; ++r) {
@@ -377,13 +381,14 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.x = x;
     prm.offsets = offsets;
     prm.perm = perm;
-    if (!grouped)
+    if (!grouped && !gather)  // the gather mode has no receive buffers (recv may be NULL)
         for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
     prm.Y = Y;
     prm.H = H;
     prm.glu = glu ? 1 : 0;
     prm.F = plan->N / 2;
     prm.a_ready = grouped ? 1 : 0;
+    prm.gather = gather ? 1 : 0;
     prm.hdr = reinterpret_cast<uint32_t*>(ws);
     prm.flags = reinterpret_cast<uint32_t*>(ws + plan->ws.flags_off);
     prm.chunk_cnt = reinterpret_cast<uint32_t*>(ws + plan->ws.chunk_cnt_off);
@@ -394,21 +399,42 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.E = plan->E;
     prm.k = plan->k;
     prm.N = plan->N;
-    prm.R = grouped ? 1 : plan->R;
-    prm.cap = grouped ? (int)plan->S : plan->cap;
+    prm.R = (grouped || gather) ? 1 : plan->R;
+    prm.cap = (grouped || gather) ? (int)plan->S : plan->cap;
     prm.tile_n = plan->tile_n;
     const int tile_cols = glu ? plan->tile_n / 2 : plan->tile_n;  // output columns per tile
     const int out_cols = glu ? plan->N / 2 : plan->N;
     prm.n_tiles = (out_cols + tile_cols - 1) / tile_cols;
     prm.k_blocks = plan->d / kTileK;
-    prm.producer_ctas = grouped ? 0 : plan->producer_ctas;
+    prm.producer_ctas = (grouped || gather) ? 0 : plan->producer_ctas;
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
-    const cudaError_t lerr =
-        plan->pair ? launch_dispatch_gemm_pair(prm, plan->num_ctas, plan->smem, static_cast<cudaStream_t>(stream))
-                   : launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t lerr;
+    if (gather && plan->pair) {
+        // the direct gather runs in the single-CTA kernel: 256-wide tiles, 4 stages
+        const size_t smem = dispatch_gemm_smem_bytes(256, 4);
+        {
+            std::lock_guard<std::mutex> lock(plan->mu);
+            if (!plan->single_ready) {
+                if (dispatch_gemm_prepare_attributes(256, 4, smem) != cudaSuccess) {
+                    cudaGetLastError();
+                    return MOE_ERR_CUDA;
+                }
+                plan->single_ready = true;
+            }
+        }
+        prm.tile_n = 256;
+        prm.n_tiles = (plan->N + 255) / 256;
+        const int grid = plan->shape.num_ctas != 0 ? std::min(plan->shape.num_ctas, plan->sm_count)
+                                                   : plan->sm_count;
+        lerr = launch_dispatch_gemm(prm, grid, 4, smem, static_cast<cudaStream_t>(stream));
+    } else if (plan->pair) {
+        lerr = launch_dispatch_gemm_pair(prm, plan->num_ctas, plan->smem, static_cast<cudaStream_t>(stream));
+    } else {
+        lerr = launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,
+                                    static_cast<cudaStream_t>(stream));
+    }
     if (lerr != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
@@ -432,6 +458,13 @@ moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x, const 
                                       uint16_t* H, void* workspace, int32_t* dev_status,
                                       void* stream) {
     return run_gemm(plan, GemmMode::kDispatchSwiglu, x, offsets, perm, W1, recv, nullptr, nullptr, H,
+                    workspace, dev_status, stream);
+}
+
+moe_status_t moe_gather_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                             const int32_t* perm, const uint16_t* W, float* Y, void* workspace,
+                             int32_t* dev_status, void* stream) {
+    return run_gemm(plan, GemmMode::kGather, x, offsets, perm, W, nullptr, nullptr, Y, nullptr,
                     workspace, dev_status, stream);
 }
 

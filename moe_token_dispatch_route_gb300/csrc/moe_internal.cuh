@@ -98,6 +98,8 @@ struct DispatchGemmParams {
     int F;                          // N/2 when glu
     uint16_t* H;                    // glu: bf16 [S][F], silu(gate) * up
     int a_ready;                    // 1: A rows are already in a_map[0] (no scatter, no flags)
+    int gather;                     // 1: A rows are copied from x by perm into shared memory
+                                    //    (no receive buffers, no scatter, no flags)
 };
 
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
@@ -175,6 +177,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// src_bytes (0 or 16) bytes are read; the rest of the 16 are filled with zeros
+__device__ __forceinline__ void cp_async16_cg_zfill(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() {

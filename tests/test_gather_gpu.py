@@ -1,0 +1,118 @@
+"""Direct-gather grouped GEMM (moe_gather_gemm) on the GPU.
+
+The A rows come straight from x (row perm[i] / k for destination row i) into
+the GEMM's shared-memory tiles; no receive buffer is written.  Each output
+element is reduced in the same order as in moe_dispatch_gemm with the same
+tile shape, so the two agree bit for bit; both are also checked against the
+oracle.
+"""
+import pytest
+import torch
+
+import oracle
+from moe_token_dispatch_route_gb300 import binding, workloads
+from tests.gpu_util import check_route, check_Y, check_Y_sampled, sample_rows_cols
+
+pytestmark = pytest.mark.gpu
+
+
+def _both(wl, inp, **plan_kw):
+    """Route once, then run the dispatch and the gather entry points on one plan."""
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **plan_kw)
+    bufs = binding.MoeBuffers(plan, "cuda")
+    x, L = inp["x"].cuda(), inp["logits"].cuda()
+    W = inp["W"] if inp["W"].is_cuda else inp["W"].cuda()
+    binding.route(plan, L, bufs)
+    bufs.Y.fill_(float("nan"))
+    binding.gather_gemm(plan, x, W, bufs)
+    rc, status = binding.moe_read_status(bufs.status)
+    assert rc == 0, status
+    Y_gather = bufs.Y.clone()
+    bufs.Y.fill_(float("nan"))
+    binding.dispatch_gemm(plan, x, W, bufs)
+    rc, status = binding.moe_read_status(bufs.status)
+    assert rc == 0, status
+    return plan, bufs, Y_gather
+
+
+@pytest.mark.parametrize("T,d,E,k,N,R,bias", [
+    (100, 128, 3, 2, 272, 1, "none"),     # ragged rows and column tail
+    (300, 64, 4, 1, 16, 1, "none"),       # minimum d and N
+    (600, 128, 16, 4, 384, 4, "zipf"),    # skewed load, empty experts, four ranks
+    (64, 256, 128, 8, 256, 1, "hot4"),    # decode-like
+    (1, 128, 8, 8, 128, 8, "none"),       # one token, k = E
+    (500, 128, 1, 1, 256, 1, "none"),     # one expert: a plain GEMM with 4 row tiles
+    (700, 256, 8, 2, 704, 1, "none"),
+])
+def test_gather_matches_dispatch_bitwise_and_oracle(monkeypatch, T, d, E, k, N, R, bias):
+    monkeypatch.setenv("MOE_PAIR", "0")
+    wl = workloads.custom("gat", T, d, E, k, N, R, bias)
+    inp = workloads.make_inputs(wl, seed=20)
+    plan, bufs, Y_gather = _both(wl, inp)
+    assert torch.equal(Y_gather, bufs.Y)
+    ref = oracle.route(inp["logits"].numpy(), k)
+    check_route(bufs, ref, k)
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], k)
+    Yref = oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"])
+    check_Y(Y_gather.cpu().double().numpy(), Yref)
+
+
+@pytest.mark.parametrize("tile_n", [128, 192])
+def test_gather_other_tile_widths(monkeypatch, tile_n):
+    monkeypatch.setenv("MOE_PAIR", "0")
+    wl = workloads.custom("gtn", 700, 256, 8, 2, 704, 1, "zipf")
+    inp = workloads.make_inputs(wl, seed=21)
+    _, bufs, Y_gather = _both(wl, inp, tile_n=tile_n)
+    assert torch.equal(Y_gather, bufs.Y)
+
+
+@pytest.mark.parametrize("T,d,E,k,N", [
+    (1500, 128, 4, 2, 512),     # several 256-row tiles per expert
+    (1000, 128, 2, 1, 400),     # ragged column tail
+])
+def test_gather_on_a_pair_plan_uses_256_wide_single_tiles(monkeypatch, T, d, E, k, N):
+    """A CTA-pair plan runs the gather in the single-CTA kernel with 256-wide
+    tiles: bit for bit the single-CTA dispatch with tile_n = 256."""
+    wl = workloads.custom("gpair", T, d, E, k, N, 1, "none")
+    inp = workloads.make_inputs(wl, seed=22)
+    monkeypatch.setenv("MOE_PAIR", "1")
+    plan, bufs, Y_gather = _both(wl, inp)
+    assert plan.info["tile_m"] == 256
+    monkeypatch.setenv("MOE_PAIR", "0")
+    _, bufs1, _ = _both(wl, inp, tile_n=256)
+    assert torch.equal(Y_gather, bufs1.Y)
+
+
+def test_gather_repeated_calls_and_grid_sizes(monkeypatch):
+    monkeypatch.setenv("MOE_PAIR", "0")
+    wl = workloads.custom("grep", 900, 256, 8, 2, 512, 2, "none")
+    inp = workloads.make_inputs(wl, seed=23)
+    outs = []
+    for kw in (dict(), dict(num_ctas=16), dict(num_ctas=3)):
+        plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **kw)
+        bufs = binding.MoeBuffers(plan, "cuda")
+        x, W, L = inp["x"].cuda(), inp["W"].cuda(), inp["logits"].cuda()
+        binding.route(plan, L, bufs)
+        for _ in range(3):
+            bufs.Y.fill_(float("nan"))
+            binding.gather_gemm(plan, x, W, bufs)
+            rc, status = binding.moe_read_status(bufs.status)
+            assert rc == 0, status
+            outs.append(bufs.Y.clone())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "finegrained", "deepseek_v3", "decode"])
+def test_gather_full_size(name):
+    """In the launch configuration of the benchmark (the plan's own choice);
+    bit for bit against the single-CTA dispatch with the same tiles."""
+    wl = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
+    plan, bufs, Y_gather = _both(wl, inp)
+    if plan.info["tile_m"] == 128:
+        assert torch.equal(Y_gather, bufs.Y)
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    check_route(bufs, ref, wl.k)
+    rows, cols = sample_rows_cols(ref, wl.N, tile_n=plan.info["tile_n"])
+    check_Y_sampled(Y_gather, workloads.bf16_bits(inp["x"]), inp["W"], ref, wl.k, rows, cols)
