@@ -212,57 +212,138 @@ constexpr int scatter_slots_per_lane(size_t bytes) {
 constexpr int kPieceVecsMax = 512;
 constexpr int kPublishBatch = 4;  // finished units per fence + publication
 
+// The warp's walk over its units (c, c + stride, c + 2 stride, ...).  The
+// units' metadata is fetched 32 units at a time, one unit per lane, so the
+// dependent loads (offsets, then perm) cost one round trip per 32 units rather
+// than one per unit; the current unit's fields are broadcast from its lane.
 struct UnitCursor {
-    int c, stride, total;
-    int e, j, seg0, cnt, nrows, rank, rbase;
-    int r, q;       // row of the unit and piece of the row
-    int tok, local; // lane r (< nrows) holds row r's token (-1: skip the row) and rank-local row
+    int c, stride, total;  // current unit (lane-uniform)
+    int slot;              // lane holding the current unit's metadata
     bool done;
+    // current unit, lane-uniform
+    int e, j, nrows, rank;
+    int r, q;              // row of the unit and piece of the row
+    // this lane's unit of the batch
+    int m_e, m_j, m_nrows, m_rank;
+    int m_tok[kRowsPerChunk];    // token of each row (-1: skip the row)
+    int m_local[kRowsPerChunk];  // row inside the rank buffer
 };
 
-__device__ void cursor_load_unit(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base,
-                                 uint32_t epoch, int lane) {
-    u.done = u.c >= u.total;
-    if (u.done) return;
-    u.e = expert_of(unit_base, p.E, u.c);
-    u.j = u.c - unit_base[u.e];
-    u.seg0 = __ldg(p.offsets + u.e);
-    u.cnt = __ldg(p.offsets + u.e + 1) - u.seg0;
-    u.nrows = min(kRowsPerChunk, u.cnt - u.j * kRowsPerChunk);
+__device__ void cursor_fetch_batch(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base,
+                                   uint32_t epoch, int lane) {
+    const int c = u.c + lane * u.stride;
+    u.m_nrows = 0;
+    u.m_e = u.m_j = u.m_rank = 0;
+#pragma unroll
+    for (int r = 0; r < kRowsPerChunk; ++r) {
+        u.m_tok[r] = -1;
+        u.m_local[r] = -1;
+    }
+    if (c >= u.total) return;
+    const int e = expert_of(unit_base, p.E, c);
+    const int j = c - unit_base[e];
+    const int seg0 = __ldg(p.offsets + e);
+    const int cnt = __ldg(p.offsets + e + 1) - seg0;
     const int e_per_rank = p.E / p.R;
-    u.rank = u.e / e_per_rank;
-    u.rbase = __ldg(p.offsets + u.rank * e_per_rank);
-    u.r = 0;
-    u.q = 0;
-    u.tok = -1;
-    u.local = -1;
-    if (lane < u.nrows) {
-        const int row = u.seg0 + u.j * kRowsPerChunk + lane;
-        u.local = row - u.rbase;
-        u.tok = __ldg(p.perm + row) / p.k;
-        if (u.local >= p.cap) {
-            report_error(p.status, kStCapacity, row, u.rank, (int)epoch);
-            u.tok = -1;
-        } else if (u.tok < 0 || u.tok >= p.T) {
+    const int rank = e / e_per_rank;
+    const int rbase = __ldg(p.offsets + rank * e_per_rank);
+    const int nrows = min(kRowsPerChunk, cnt - j * kRowsPerChunk);
+    u.m_e = e;
+    u.m_j = j;
+    u.m_rank = rank;
+    u.m_nrows = nrows;
+    int perm_v[kRowsPerChunk];
+#pragma unroll
+    for (int r = 0; r < kRowsPerChunk; ++r)
+        perm_v[r] = r < nrows ? __ldg(p.perm + seg0 + j * kRowsPerChunk + r) : 0;
+#pragma unroll
+    for (int r = 0; r < kRowsPerChunk; ++r) {
+        if (r >= nrows) continue;
+        const int row = seg0 + j * kRowsPerChunk + r;
+        const int local = row - rbase;
+        const int tok = perm_v[r] / p.k;
+        if (local >= p.cap) {
+            report_error(p.status, kStCapacity, row, rank, (int)epoch);
+        } else if (tok < 0 || tok >= p.T) {
             report_error(p.status, kStDevice, -3, row, (int)epoch);
-            u.tok = -1;
+        } else {
+            u.m_tok[r] = tok;
+            u.m_local[r] = local;
         }
     }
 }
 
-__device__ void publish_unit(const DispatchGemmParams& p, const int* mt_base, int e, int j,
-                             uint32_t epoch) {
-    const int cnt = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-    const int m = j / kChunksPerTile;
-    const int mtile = mt_base[e] + m;
-    const int units_in_tile =
-        min(kChunksPerTile, (cnt + kRowsPerChunk - 1) / kRowsPerChunk - m * kChunksPerTile);
-    const uint32_t prev = atomicAdd(p.chunk_cnt + mtile, 1u);
-    if (prev + 1u == (uint32_t)units_in_tile) {
-        __threadfence();
-        p.chunk_cnt[mtile] = 0u;  // ready for the next call
-        fence_proxy_async_global();
-        if (mtile != p.skip_publish) st_release_gpu(p.flags + mtile, epoch);
+__device__ void cursor_select(UnitCursor& u) {
+    u.done = u.c >= u.total;
+    u.e = __shfl_sync(kFull, u.m_e, u.slot);
+    u.j = __shfl_sync(kFull, u.m_j, u.slot);
+    u.nrows = __shfl_sync(kFull, u.m_nrows, u.slot);
+    u.rank = __shfl_sync(kFull, u.m_rank, u.slot);
+    u.r = 0;
+    u.q = 0;
+}
+
+// first unit of the walk
+__device__ void cursor_init(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base, int first,
+                            int stride, uint32_t epoch, int lane) {
+    u.c = first;
+    u.stride = stride;
+    u.total = unit_base[p.E];
+    u.slot = 0;
+    cursor_fetch_batch(u, p, unit_base, epoch, lane);
+    cursor_select(u);
+}
+
+// next unit of the walk
+__device__ void cursor_next(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base,
+                            uint32_t epoch, int lane) {
+    u.c += u.stride;
+    if (++u.slot == 32) {
+        u.slot = 0;
+        cursor_fetch_batch(u, p, unit_base, epoch, lane);
+    }
+    cursor_select(u);
+}
+
+// token and rank-buffer row of row r of the current unit (lane-uniform)
+__device__ __forceinline__ void cursor_row(const UnitCursor& u, int r, int& tok, int& local) {
+    int t = u.m_tok[0], l = u.m_local[0];
+#pragma unroll
+    for (int i = 1; i < kRowsPerChunk; ++i)
+        if (r == i) {
+            t = u.m_tok[i];
+            l = u.m_local[i];
+        }
+    tok = __shfl_sync(kFull, t, u.slot);
+    local = __shfl_sync(kFull, l, u.slot);
+}
+
+// Counts `n` finished units in (their rows already written and fenced by the
+// caller).  The per-tile counters are incremented first, all n together, so
+// their round trips overlap; the unit that completes a tile then releases the
+// tile's ready flag with the call's epoch and returns the counter to zero.
+__device__ void publish_units(const DispatchGemmParams& p, const int* mt_base, const int* es,
+                              const int* js, int n, uint32_t epoch) {
+    uint32_t prev[kPublishBatch];
+    int mtile[kPublishBatch], units[kPublishBatch];
+#pragma unroll
+    for (int i = 0; i < kPublishBatch; ++i) {
+        if (i >= n) break;
+        const int cnt = __ldg(p.offsets + es[i] + 1) - __ldg(p.offsets + es[i]);
+        const int m = js[i] / kChunksPerTile;
+        mtile[i] = mt_base[es[i]] + m;
+        units[i] = min(kChunksPerTile, (cnt + kRowsPerChunk - 1) / kRowsPerChunk - m * kChunksPerTile);
+        prev[i] = atomicAdd(p.chunk_cnt + mtile[i], 1u);
+    }
+#pragma unroll
+    for (int i = 0; i < kPublishBatch; ++i) {
+        if (i >= n) break;
+        if (prev[i] + 1u == (uint32_t)units[i]) {
+            __threadfence();
+            p.chunk_cnt[mtile[i]] = 0u;  // ready for the next call
+            fence_proxy_async_global();
+            if (mtile[i] != p.skip_publish) st_release_gpu(p.flags + mtile[i], epoch);
+        }
     }
 }
 
@@ -282,10 +363,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
     PieceRec* ring = ctl->piece[warp];
 
     UnitCursor L;
-    L.c = role * (kThreads / 32) + warp;
-    L.stride = nwarps;
-    L.total = unit_base[p.E];
-    cursor_load_unit(L, p, unit_base, epoch, lane);
+    cursor_init(L, p, unit_base, role * (kThreads / 32) + warp, nwarps, epoch, lane);
 
     int pend_e[kPublishBatch], pend_j[kPublishBatch];
     int npend = 0;
@@ -294,8 +372,8 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
         // keep up to nbuf - 1 pieces loading
         while (!L.done && gi - gd < nbuf - 1) {
             const int b = (int)(gi % nbuf);
-            const int tr = __shfl_sync(kFull, L.tok, L.r);
-            const int lr = __shfl_sync(kFull, L.local, L.r);
+            int tr, lr;
+            cursor_row(L, L.r, tr, lr);
             const int q0 = L.q * piece_vecs;
             const int q1 = min(q0 + piece_vecs, nvec);
             if (tr >= 0) {
@@ -322,10 +400,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
             ++gi;
             if (++L.q == pieces_per_row) {
                 L.q = 0;
-                if (++L.r == L.nrows) {
-                    L.c += L.stride;
-                    cursor_load_unit(L, p, unit_base, epoch, lane);
-                }
+                if (++L.r == L.nrows) cursor_next(L, p, unit_base, epoch, lane);
             }
         }
         if (gd == gi) break;
@@ -358,7 +433,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
             __syncwarp();
             if (lane == 0) {
                 __threadfence();
-                for (int i = 0; i < npend; ++i) publish_unit(p, mt_base, pend_e[i], pend_j[i], epoch);
+                publish_units(p, mt_base, pend_e, pend_j, npend, epoch);
             }
             npend = 0;
         }
@@ -859,6 +934,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t epoch = ctl->epoch;
     const int role = ctl->role;
 
+    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
+    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
     if (role < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
@@ -867,8 +944,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }
 
-    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
-    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
     if (warp == 0) {
         if (lane == 0) tma_role<BN, STAGES>(p, ctl, mt_base, sA, sB, w);
         __syncwarp();
@@ -1247,6 +1322,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t epoch = ctl->epoch;
     const int scatter_index = 2 * ctl->role + (int)(rank & 1u);
 
+    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
+    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
     if (scatter_index < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
@@ -1255,8 +1332,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
     }
 
-    const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
-    const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
     if (warp == 0) {
         if (lane == 0) pair_tma_role<STAGES>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
         __syncwarp();
