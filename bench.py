@@ -421,6 +421,27 @@ def run_ours(args, wl):
     gather_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in gev)
     binding.dispatch_gemm(plan, x, W, bufs, stream)  # leave Y as the path computes it
 
+    # the fused kernel with a bf16 Y (MOE_OUT_BF16), timed on its own
+    plan_b = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n,
+                              producer_ctas=args.producer_ctas, out_dtype=binding.MOE_OUT_BF16,
+                              device=local)
+    bufs_b = binding.MoeBuffers(plan_b, dev)
+    binding.route(plan_b, logits, bufs_b, stream)
+    for _ in range(3):
+        binding.dispatch_gemm(plan_b, x, W, bufs_b, stream)
+    bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for a_, b_ in bev:
+        flush.fill_(1.0)
+        a_.record(stream)
+        binding.dispatch_gemm(plan_b, x, W, bufs_b, stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    rc, st = binding.moe_read_status(bufs_b.status, stream)
+    if rc != 0:
+        raise SystemExit(f"device status after the bf16-output timing: {st}")
+    ybf16_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in bev)
+    del bufs_b, plan_b
+
     ffn = None
     if args.ffn == "on" or (args.ffn == "auto" and wl.name == "mixtral"):
         ffn = time_swiglu_ffn(wl, inp, x, logits, dev, stream, flush)
@@ -509,6 +530,9 @@ def run_ours(args, wl):
                           "note": "moe_gather_gemm: A rows copied from x by perm straight into the "
                                   "GEMM's shared memory, no receive buffers (single-CTA kernel); "
                                   "20 launches, L2 flushed; not in value"},
+        "y_bf16": {"ms": ybf16_ms, "tflops": flops / (ybf16_ms * 1e9),
+                   "note": "moe_dispatch_gemm with out_dtype = MOE_OUT_BF16 (Y rounded once to bf16, "
+                           "half the Y bytes); 20 launches, L2 flushed; not in value"},
         "swiglu_ffn": ffn,
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

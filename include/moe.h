@@ -97,7 +97,17 @@ typedef struct moe_shape {
                                    over all E logits.  MOE_ROUTE_SIGMOID: logistic of
                                    each logit instead; MOE_ROUTE_RENORM: each token's k
                                    gates divided by their sum.  Other bits must be 0.   */
+    int32_t tile_m;             /* GEMM tile height: 0 = auto; 128 = one CTA per tile;
+                                   256 = CTA pairs (tcgen05 cta_group::2; needs N >= 256
+                                   and tile_n 0 or 256)                                  */
+    int32_t out_dtype;          /* element type of Y: MOE_OUT_F32 (0, default) or
+                                   MOE_OUT_BF16 (fp32 accumulation rounded once to bf16,
+                                   nearest even)                                         */
 } moe_shape_t;
+
+/* moe_shape_t.out_dtype */
+#define MOE_OUT_F32 0
+#define MOE_OUT_BF16 1
 
 typedef struct moe_plan_info {
     int32_t tile_m, tile_n, tile_k;   /* GEMM tile (rows, columns, reduction step); rows =
@@ -194,8 +204,9 @@ MOE_API moe_status_t moe_route_biased(moe_plan_t plan, const float* logits,
  *                 buffer, bf16 [rank_capacity_rows][d].  Rank r owns experts
  *                 [r*E/R, (r+1)*E/R); its buffer receives the destination rows
  *                 [offsets[r*E/R], offsets[(r+1)*E/R]) in order (out).
- *   Y        out: fp32 [S][N]; Y[i] = recv row of destination row i times
- *                 W[e(i)], where e(i) is the expert whose segment holds i.
+ *   Y        out: [S][N], fp32 (or bf16 with MOE_OUT_BF16 in the plan's shape);
+ *                 Y[i] = recv row of destination row i times W[e(i)], where
+ *                 e(i) is the expert whose segment holds i.
  *                 Row order is the destination (expert-sorted) order; undoing
  *                 the permutation is the caller's step.
  *   workspace in/out: the plan's workspace.
@@ -206,7 +217,7 @@ MOE_API moe_status_t moe_route_biased(moe_plan_t plan, const float* logits,
  */
 MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
                                const int32_t* offsets, const int32_t* perm,
-                               const uint16_t* W, void* const* recv, float* Y,
+                               const uint16_t* W, void* const* recv, void* Y,
                                void* workspace, int32_t* dev_status, void* stream);
 
 /*
@@ -244,7 +255,7 @@ MOE_API moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x
  *   moe_dispatch_gemm.  No receive buffers.  Launches one kernel.
  */
 MOE_API moe_status_t moe_gather_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
-                                     const int32_t* perm, const uint16_t* W, float* Y,
+                                     const int32_t* perm, const uint16_t* W, void* Y,
                                      void* workspace, int32_t* dev_status, void* stream);
 
 /*
@@ -256,12 +267,12 @@ MOE_API moe_status_t moe_gather_gemm(moe_plan_t plan, const uint16_t* x, const i
  *   offsets  in:  int32 [E+1]: expert e owns rows [offsets[e], offsets[e+1]);
  *                 offsets[E] must equal S = T*k.
  *   W        in:  bf16 [E][d][N].
- *   Y        out: fp32 [S][N]; Y[i] = A[i] x W[e(i)].
+ *   Y        out: [S][N] in the plan's out_dtype; Y[i] = A[i] x W[e(i)].
  * Workspace and status as for moe_dispatch_gemm (the plan's workspace; a plan
  * may serve both entry points on one stream).  Launches one kernel.
  */
 MOE_API moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const int32_t* offsets,
-                                      const uint16_t* W, float* Y, void* workspace,
+                                      const uint16_t* W, void* Y, void* workspace,
                                       int32_t* dev_status, void* stream);
 
 /*
@@ -285,14 +296,15 @@ MOE_API moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const
  * weight each token's k expert outputs by its gates.  The articles' table row
  * "MoE Dispatch + GEMM" describes the dispatch side only; the combine is the
  * mirror image that completes the layer's output.
- *   Y      in:  fp32 [S][N] from moe_dispatch_gemm (destination order).
+ *   Y      in:  [S][N] from moe_dispatch_gemm (destination order), fp32 or bf16
+ *                as the plan's out_dtype says.
  *   topk_w in:  fp32 [T][k] from moe_route.
  *   dest   in:  int32 [S] from moe_route.
  *   out    out: fp32 [T][N]; out[t][n] = sum_{j<k} topk_w[t][j] * Y[dest[t*k+j]][n],
  *               fp32 fused multiply-adds in ascending j (identical on every run).
  * Launches one kernel on `stream`; no workspace.
  */
-MOE_API moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w,
+MOE_API moe_status_t moe_combine(moe_plan_t plan, const void* Y, const float* topk_w,
                                  const int32_t* dest, float* out, void* stream);
 
 /*

@@ -31,6 +31,8 @@ MOE_ERR_CAPACITY = 6
 MOE_ERR_DEVICE = 7
 MOE_ROUTE_RENORM = 1
 MOE_ROUTE_SIGMOID = 2
+MOE_OUT_F32 = 0
+MOE_OUT_BF16 = 1
 
 
 class MoeError(RuntimeError):
@@ -46,7 +48,7 @@ class Shape(ctypes.Structure):
         ("rank_capacity_rows", ctypes.c_int32), ("tile_n", ctypes.c_int32),
         ("producer_ctas", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
         ("timeout_ns", ctypes.c_int64), ("debug_skip_publish", ctypes.c_int32),
-        ("route_flags", ctypes.c_int32),
+        ("route_flags", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
     ]
 
 
@@ -154,11 +156,12 @@ class Plan:
 def moe_plan(T: int, d: int, E: int, k: int, N: int, num_ranks: int = 1,
              rank_capacity_rows: int = 0, tile_n: int = 0, producer_ctas: int = 0,
              num_ctas: int = 0, timeout_ns: int = 0, debug_skip_publish: int = 0,
-             route_flags: int = 0, device: int | None = None) -> Plan:
+             route_flags: int = 0, tile_m: int = 0, out_dtype: int = MOE_OUT_F32,
+             device: int | None = None) -> Plan:
     lib = load_library()
     dev = torch.cuda.current_device() if device is None else int(device)
     shape = Shape(T, d, E, k, N, num_ranks, rank_capacity_rows, tile_n, producer_ctas, num_ctas,
-                  timeout_ns, debug_skip_publish, route_flags)
+                  timeout_ns, debug_skip_publish, route_flags, tile_m, out_dtype)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib.moe_plan(ctypes.byref(shape), dev, ctypes.byref(handle), ctypes.byref(ws)), "moe_plan")
@@ -272,7 +275,8 @@ class MoeBuffers:
         self.perm = torch.empty(S, **i32)
         self.dest = torch.empty(S, **i32)
         self.recv = [torch.empty(max(cap, 1), s.d, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-        self.Y = torch.empty(S, s.N, dtype=torch.float32, device=dev) if out == "Y" else None
+        y_dtype = torch.bfloat16 if s.out_dtype == MOE_OUT_BF16 else torch.float32
+        self.Y = torch.empty(S, s.N, dtype=y_dtype, device=dev) if out == "Y" else None
         self.H = torch.empty(S, s.N // 2, dtype=torch.bfloat16, device=dev) if out == "H" else None
         self.workspace = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
         self.status = torch.zeros(4, **i32)

@@ -3,7 +3,8 @@
 // destination permutation and weights each token's k expert outputs by its gates:
 //   out[t][n] = sum_{j<k} w[t*k+j] * Y[dest[t*k+j]][n]
 // in fp32 with fused multiply-adds in ascending j, so the result is the same on
-// every run.  HBM-bound: it reads T*k rows of Y (gathered) and writes T rows.
+// every run.  HBM-bound: it reads T*k rows of Y (gathered; fp32 or bf16, whose
+// values are exactly representable in fp32) and writes T rows.
 //
 // One CTA per (token, block of 1024 columns); each thread owns 4 consecutive
 // columns and keeps its k gathered 16-byte loads in flight.
@@ -30,7 +31,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
             const int row = __ldg(a.dest + s);
             if (row < 0 || row >= a.S) continue;
             const float wj = __ldg(a.w + s);
-            const float4 y = __ldcs(reinterpret_cast<const float4*>(a.Y + (size_t)row * a.N + n));
+            float4 y;
+            if (a.y_bf16) {
+                const uint2 h = __ldcs(reinterpret_cast<const uint2*>(
+                    static_cast<const uint16_t*>(a.Y) + (size_t)row * a.N + n));
+                y = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u),
+                                __uint_as_float(h.y << 16), __uint_as_float(h.y & 0xFFFF0000u));
+            } else {
+                y = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(a.Y) + (size_t)row * a.N + n));
+            }
             acc.x = fmaf(wj, y.x, acc.x);
             acc.y = fmaf(wj, y.y, acc.y);
             acc.z = fmaf(wj, y.z, acc.z);

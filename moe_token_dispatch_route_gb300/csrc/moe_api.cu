@@ -99,7 +99,8 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 moe_status_t validate_shape(const moe_shape_t& s) {
     if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.k <= 0 || s.N <= 0 || s.num_ranks < 0 ||
         s.rank_capacity_rows < 0 || s.producer_ctas < 0 || s.num_ctas < 0 || s.timeout_ns < 0 ||
-        s.debug_skip_publish < 0 || (s.route_flags & ~(MOE_ROUTE_RENORM | MOE_ROUTE_SIGMOID)) != 0)
+        s.debug_skip_publish < 0 || (s.route_flags & ~(MOE_ROUTE_RENORM | MOE_ROUTE_SIGMOID)) != 0 ||
+        (s.out_dtype != MOE_OUT_F32 && s.out_dtype != MOE_OUT_BF16))
         return MOE_ERR_INVALID_ARG;
     const int R = s.num_ranks == 0 ? 1 : s.num_ranks;
     if (s.E > kMaxE || s.k > std::min(s.E, 32)) return MOE_ERR_UNSUPPORTED;
@@ -108,6 +109,8 @@ moe_status_t validate_shape(const moe_shape_t& s) {
     if (R > kMaxRanks || s.E % R != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s.T * s.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 192 && s.tile_n != 256) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_m != 0 && s.tile_m != 128 && s.tile_m != 256) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_m == 256 && (s.N < 256 || (s.tile_n != 0 && s.tile_n != 256))) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -188,15 +191,21 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     }
     p->num_ctas = shape->num_ctas != 0 ? std::min(shape->num_ctas, sms) : sms;
     // CTA pairs for layers with many rows per expert (on average at least one 256-row
-    // tile) and full-width tiles; MOE_PAIR=0/1 overrides the choice for tuning sweeps
-    p->pair = p->S >= 256LL * p->E && p->N >= 256 && (shape->tile_n == 0 || shape->tile_n == 256);
-    if (const char* env = std::getenv("MOE_PAIR")) p->pair = std::atoi(env) != 0 && p->N >= 256;
+    // tile) and full-width tiles, unless the shape fixes tile_m
+    if (shape->tile_m == 0)
+        p->pair = p->S >= 256LL * p->E && p->N >= 256 && (shape->tile_n == 0 || shape->tile_n == 256);
+    else
+        p->pair = shape->tile_m == 256;
     if (p->pair) {
         int max_clusters = 0;
         p->smem = dispatch_gemm_pair_smem_bytes();
         if ((int)p->smem > smem_optin ||
             dispatch_gemm_pair_prepare(p->smem, &max_clusters) != cudaSuccess || max_clusters < 1) {
             cudaGetLastError();
+            if (shape->tile_m == 256) {  // pairs were asked for and cannot run here
+                delete p;
+                return MOE_ERR_UNSUPPORTED;
+            }
             p->pair = false;  // no co-resident pairs: keep the single-CTA kernel
             p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
         } else {
@@ -325,7 +334,7 @@ enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped, kGather };
 // as they land; kGrouped computes on rows the caller has already laid out.
 moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const int32_t* offsets,
                       const int32_t* perm, const uint16_t* W, void* const* recv, const uint16_t* A,
-                      float* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream) {
+                      void* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
@@ -384,6 +393,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     if (!grouped && !gather)  // the gather mode has no receive buffers (recv may be NULL)
         for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
     prm.Y = Y;
+    prm.out_bf16 = plan->shape.out_dtype == MOE_OUT_BF16 ? 1 : 0;
     prm.H = H;
     prm.glu = glu ? 1 : 0;
     prm.F = plan->N / 2;
@@ -447,7 +457,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
 extern "C" {
 
 moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
-                               const int32_t* perm, const uint16_t* W, void* const* recv, float* Y,
+                               const int32_t* perm, const uint16_t* W, void* const* recv, void* Y,
                                void* workspace, int32_t* dev_status, void* stream) {
     return run_gemm(plan, GemmMode::kDispatch, x, offsets, perm, W, recv, nullptr, Y, nullptr,
                     workspace, dev_status, stream);
@@ -462,14 +472,14 @@ moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x, const 
 }
 
 moe_status_t moe_gather_gemm(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
-                             const int32_t* perm, const uint16_t* W, float* Y, void* workspace,
+                             const int32_t* perm, const uint16_t* W, void* Y, void* workspace,
                              int32_t* dev_status, void* stream) {
     return run_gemm(plan, GemmMode::kGather, x, offsets, perm, W, nullptr, nullptr, Y, nullptr,
                     workspace, dev_status, stream);
 }
 
 moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const int32_t* offsets,
-                              const uint16_t* W, float* Y, void* workspace, int32_t* dev_status,
+                              const uint16_t* W, void* Y, void* workspace, int32_t* dev_status,
                               void* stream) {
     return run_gemm(plan, GemmMode::kGrouped, nullptr, offsets, nullptr, W, nullptr, A, Y, nullptr,
                     workspace, dev_status, stream);
@@ -500,7 +510,7 @@ moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_
     return MOE_OK;
 }
 
-moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w, const int32_t* dest,
+moe_status_t moe_combine(moe_plan_t plan, const void* Y, const float* topk_w, const int32_t* dest,
                          float* out, void* stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     if (plan->T == 0) return MOE_OK;
@@ -511,6 +521,7 @@ moe_status_t moe_combine(moe_plan_t plan, const float* Y, const float* topk_w, c
     if (!guard.ok) return MOE_ERR_CUDA;
     CombineArgs a;
     a.Y = Y;
+    a.y_bf16 = plan->shape.out_dtype == MOE_OUT_BF16 ? 1 : 0;
     a.w = topk_w;
     a.dest = dest;
     a.out = out;

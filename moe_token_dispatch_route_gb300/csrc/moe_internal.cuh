@@ -82,7 +82,7 @@ struct DispatchGemmParams {
     const int32_t* offsets;
     const int32_t* perm;
     uint16_t* recv[kMaxRanks];
-    float* Y;
+    void* Y;                        // fp32, or bf16 when out_bf16
     uint32_t* hdr;
     uint32_t* flags;
     uint32_t* chunk_cnt;
@@ -100,6 +100,7 @@ struct DispatchGemmParams {
     int a_ready;                    // 1: A rows are already in a_map[0] (no scatter, no flags)
     int gather;                     // 1: A rows are copied from x by perm into shared memory
                                     //    (no receive buffers, no scatter, no flags)
+    int out_bf16;                   // 1: Y is bf16 (fp32 accumulator rounded once)
 };
 
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
@@ -116,7 +117,8 @@ struct RouterArgs {
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream);
 
 struct CombineArgs {
-    const float* Y;       // [S][N] destination order
+    const void* Y;        // [S][N] destination order, fp32 or bf16
+    int y_bf16;
     const float* w;       // [T][k] gate weights
     const int32_t* dest;  // [T*k]
     float* out;           // [T][N]

@@ -56,7 +56,8 @@ def test_struct_layout_matches_header(tmp_path):
 
 def _plan_rc(lib, **kw):
     fields = dict(T=64, d=128, E=8, k=2, N=256, num_ranks=1, rank_capacity_rows=0, tile_n=0,
-                  producer_ctas=0, num_ctas=0, timeout_ns=0, debug_skip_publish=0, route_flags=0)
+                  producer_ctas=0, num_ctas=0, timeout_ns=0, debug_skip_publish=0, route_flags=0,
+                  tile_m=0, out_dtype=0)
     fields.update(kw)
     shape = binding.Shape(**fields)
     h = ctypes.c_void_p()
@@ -78,6 +79,10 @@ def _plan_rc(lib, **kw):
     (dict(num_ranks=3), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=64, num_ranks=64), binding.MOE_ERR_UNSUPPORTED),
     (dict(tile_n=160), binding.MOE_ERR_UNSUPPORTED),
+    (dict(out_dtype=2), binding.MOE_ERR_INVALID_ARG),
+    (dict(tile_m=64), binding.MOE_ERR_UNSUPPORTED),
+    (dict(tile_m=256, N=128), binding.MOE_ERR_UNSUPPORTED),
+    (dict(tile_m=256, tile_n=128), binding.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=2), binding.MOE_ERR_UNSUPPORTED),
 ])
 def test_plan_rejects_bad_shapes_before_any_device_call(lib, kw, expect):

@@ -145,7 +145,7 @@ def test_receive_capacity_overflow_is_reported():
 
 # ---------------------------------------------------------------- CTA-pair mode
 # The plan runs 256-row tiles on CTA pairs (tcgen05 cta_group::2) when experts
-# hold many rows; MOE_PAIR forces the choice either way for these tests.
+# hold many rows; the shape's tile_m fixes the choice either way for these tests.
 
 @pytest.mark.parametrize("T,d,E,k,N,R,bias", [
     (1000, 128, 2, 1, 512, 1, "none"),    # 2 experts of ~500 rows: odd 128-row halves at the tail
@@ -153,45 +153,41 @@ def test_receive_capacity_overflow_is_reported():
     (900, 128, 8, 2, 256, 4, "zipf"),     # skewed: some experts empty, some with < 128 rows
     (130, 64, 1, 1, 272, 1, "none"),      # one expert, 130 rows: the odd half holds 2 rows
 ])
-def test_pair_mode_full_parity(monkeypatch, T, d, E, k, N, R, bias):
-    monkeypatch.setenv("MOE_PAIR", "1")
-    plan, _ = _full_check(workloads.custom("pair", T, d, E, k, N, R, bias))
+def test_pair_mode_full_parity(T, d, E, k, N, R, bias):
+    plan, _ = _full_check(workloads.custom("pair", T, d, E, k, N, R, bias), tile_m=256)
     assert plan.info["tile_m"] == 256
 
 
-def test_pair_and_single_modes_agree(monkeypatch):
+def test_pair_and_single_modes_agree():
     wl = workloads.custom("modes", 1200, 256, 4, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=8)
     outs = {}
-    for mode in ("0", "1"):
-        monkeypatch.setenv("MOE_PAIR", mode)
-        plan, bufs, rc, status = run_path(wl, inp)
+    for tile_m in (128, 256):
+        plan, bufs, rc, status = run_path(wl, inp, tile_m=tile_m)
         assert rc == 0, status
-        assert plan.info["tile_m"] == (256 if mode == "1" else 128)
-        outs[mode] = bufs.Y.cpu().double().numpy()
+        assert plan.info["tile_m"] == tile_m
+        outs[tile_m] = bufs.Y.cpu().double().numpy()
     # same K order per element; the two MMA shapes may round differently, so compare to tolerance
-    err = np.abs(outs["0"] - outs["1"]).max()
-    assert err <= 1e-4 * np.sqrt(np.mean(outs["0"] ** 2))
+    err = np.abs(outs[128] - outs[256]).max()
+    assert err <= 1e-4 * np.sqrt(np.mean(outs[128] ** 2))
 
 
-def test_pair_mode_role_split_does_not_change_bits(monkeypatch):
-    monkeypatch.setenv("MOE_PAIR", "1")
+def test_pair_mode_role_split_does_not_change_bits():
     wl = workloads.custom("psplit", 1500, 128, 4, 2, 512, 1, "none")
     inp = workloads.make_inputs(wl, seed=9)
     outs = []
     for kw in (dict(), dict(producer_ctas=2), dict(producer_ctas=60), dict(num_ctas=16, producer_ctas=4)):
-        _, bufs, rc, status = run_path(wl, inp, **kw)
+        _, bufs, rc, status = run_path(wl, inp, tile_m=256, **kw)
         assert rc == 0, status
         outs.append(bufs.Y.clone())
     for o in outs[1:]:
         assert torch.equal(outs[0], o)
 
 
-def test_pair_mode_missing_flag_times_out(monkeypatch):
-    monkeypatch.setenv("MOE_PAIR", "1")
+def test_pair_mode_missing_flag_times_out():
     wl = workloads.custom("pfault", 600, 128, 2, 1, 256, 1, "none")
     inp = workloads.make_inputs(wl, seed=10)
-    plan, bufs, rc, status = run_path(wl, inp, timeout_ns=2_000_000, debug_skip_publish=2)
+    plan, bufs, rc, status = run_path(wl, inp, tile_m=256, timeout_ns=2_000_000, debug_skip_publish=2)
     assert plan.info["tile_m"] == 256
     assert rc == binding.MOE_ERR_TIMEOUT, status
     assert status[1] == 1
@@ -205,3 +201,55 @@ def test_pair_mode_missing_flag_times_out(monkeypatch):
 ])
 def test_limits_full_parity(T, d, E, k, N, R):
     _full_check(workloads.custom("limits", T, d, E, k, N, R))
+
+
+# ------------------------------------------------------------------ bf16 output
+# With MOE_OUT_BF16 the fp32 accumulator is rounded once to bf16 (nearest even):
+# at most half an ulp, 2^-8 of the value, beyond the fp32 accumulation error.
+
+def _check_bf16(Y_bf16: np.ndarray, Yref: np.ndarray):
+    assert np.isfinite(Y_bf16).all(), "unwritten (NaN) or non-finite output"
+    rms = float(np.sqrt(np.mean(Yref ** 2)))
+    assert (np.abs(Y_bf16 - Yref) <= 2.0 ** -8 * np.abs(Yref) + 1e-4 * rms).all()
+
+
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 256), (128, 128), (256, 0)])
+def test_bf16_output_full_parity_and_combine(tile_m, tile_n):
+    wl = workloads.custom("bf16", 1000, 256, 4, 2, 400, 2, "none")
+    inp = workloads.make_inputs(wl, seed=14)
+    plan, bufs, rc, status = run_path(wl, inp, tile_m=tile_m, tile_n=tile_n, out_dtype=binding.MOE_OUT_BF16)
+    assert rc == 0, status
+    assert bufs.Y.dtype == torch.bfloat16 and plan.info["tile_m"] == tile_m
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+    Yref = oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"])
+    _check_bf16(bufs.Y.float().cpu().double().numpy(), Yref)
+    # combine reads the bf16 rows: each term carries at most the rounding of its row
+    out = torch.full((wl.T, wl.N), float("nan"), device="cuda")
+    binding.moe_combine(plan, bufs.Y, bufs.topk_w, bufs.dest, out)
+    want = oracle.combine(Yref, ref["topk_w"], ref["dest"])
+    bound = oracle.combine(np.abs(Yref), np.abs(ref["topk_w"]), ref["dest"]) * 2.0 ** -8
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    assert (np.abs(out.cpu().double().numpy() - want) <= bound + 1e-4 * rms).all()
+
+
+def test_bf16_output_mixtral_full_size_sampled():
+    wl = workloads.WORKLOADS["mixtral"]
+    inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
+    plan, bufs, rc, status = run_path(wl, inp, out_dtype=binding.MOE_OUT_BF16)
+    assert rc == 0, status
+    assert not torch.isnan(bufs.Y).any().item()
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    rows, cols = sample_rows_cols(ref, wl.N, tile_n=plan.info["tile_n"])
+    a_rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"][rows], wl.k)
+    cols_t = torch.tensor(cols, device="cuda")
+    got = bufs.Y[torch.tensor(rows, device="cuda")][:, cols_t].float().cpu().double().numpy()
+    want = np.empty_like(got)
+    cache = {}
+    for i, row in enumerate(rows):
+        e = oracle.expert_of_row(ref["offsets"], row)
+        if e not in cache:
+            cache[e] = workloads.bf16_bits(inp["W"][e][:, cols_t])
+        for j in range(len(cols)):
+            want[i, j] = oracle.gemm_entry(a_rows[i], cache[e], j)
+    _check_bf16(got, want)

@@ -44,11 +44,10 @@ def _both(wl, inp, **plan_kw):
     (500, 128, 1, 1, 256, 1, "none"),     # one expert: a plain GEMM with 4 row tiles
     (700, 256, 8, 2, 704, 1, "none"),
 ])
-def test_gather_matches_dispatch_bitwise_and_oracle(monkeypatch, T, d, E, k, N, R, bias):
-    monkeypatch.setenv("MOE_PAIR", "0")
+def test_gather_matches_dispatch_bitwise_and_oracle(T, d, E, k, N, R, bias):
     wl = workloads.custom("gat", T, d, E, k, N, R, bias)
     inp = workloads.make_inputs(wl, seed=20)
-    plan, bufs, Y_gather = _both(wl, inp)
+    plan, bufs, Y_gather = _both(wl, inp, tile_m=128)
     assert torch.equal(Y_gather, bufs.Y)
     ref = oracle.route(inp["logits"].numpy(), k)
     check_route(bufs, ref, k)
@@ -58,11 +57,10 @@ def test_gather_matches_dispatch_bitwise_and_oracle(monkeypatch, T, d, E, k, N, 
 
 
 @pytest.mark.parametrize("tile_n", [128, 192])
-def test_gather_other_tile_widths(monkeypatch, tile_n):
-    monkeypatch.setenv("MOE_PAIR", "0")
+def test_gather_other_tile_widths(tile_n):
     wl = workloads.custom("gtn", 700, 256, 8, 2, 704, 1, "zipf")
     inp = workloads.make_inputs(wl, seed=21)
-    _, bufs, Y_gather = _both(wl, inp, tile_n=tile_n)
+    _, bufs, Y_gather = _both(wl, inp, tile_m=128, tile_n=tile_n)
     assert torch.equal(Y_gather, bufs.Y)
 
 
@@ -70,26 +68,23 @@ def test_gather_other_tile_widths(monkeypatch, tile_n):
     (1500, 128, 4, 2, 512),     # several 256-row tiles per expert
     (1000, 128, 2, 1, 400),     # ragged column tail
 ])
-def test_gather_on_a_pair_plan_uses_256_wide_single_tiles(monkeypatch, T, d, E, k, N):
+def test_gather_on_a_pair_plan_uses_256_wide_single_tiles(T, d, E, k, N):
     """A CTA-pair plan runs the gather in the single-CTA kernel with 256-wide
     tiles: bit for bit the single-CTA dispatch with tile_n = 256."""
     wl = workloads.custom("gpair", T, d, E, k, N, 1, "none")
     inp = workloads.make_inputs(wl, seed=22)
-    monkeypatch.setenv("MOE_PAIR", "1")
-    plan, bufs, Y_gather = _both(wl, inp)
+    plan, bufs, Y_gather = _both(wl, inp, tile_m=256)
     assert plan.info["tile_m"] == 256
-    monkeypatch.setenv("MOE_PAIR", "0")
-    _, bufs1, _ = _both(wl, inp, tile_n=256)
+    _, bufs1, _ = _both(wl, inp, tile_m=128, tile_n=256)
     assert torch.equal(Y_gather, bufs1.Y)
 
 
-def test_gather_repeated_calls_and_grid_sizes(monkeypatch):
-    monkeypatch.setenv("MOE_PAIR", "0")
+def test_gather_repeated_calls_and_grid_sizes():
     wl = workloads.custom("grep", 900, 256, 8, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=23)
     outs = []
     for kw in (dict(), dict(num_ctas=16), dict(num_ctas=3)):
-        plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **kw)
+        plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=128, **kw)
         bufs = binding.MoeBuffers(plan, "cuda")
         x, W, L = inp["x"].cuda(), inp["W"].cuda(), inp["logits"].cuda()
         binding.route(plan, L, bufs)

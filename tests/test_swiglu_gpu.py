@@ -81,9 +81,8 @@ def test_swiglu_up_full_parity(T, d, E, k, F, R, bias, tile_n):
     (1000, 128, 2, 1, 272),   # 3 column tiles of 128 (128, 128, 16); odd halves at the tail
     (130, 64, 1, 1, 128),     # one expert, 130 rows: the odd half holds 2 rows
 ])
-def test_swiglu_up_pair_mode(monkeypatch, T, d, E, k, F):
-    monkeypatch.setenv("MOE_PAIR", "1")
-    plan = _up_check(T, d, E, k, F, 1, "none")
+def test_swiglu_up_pair_mode(T, d, E, k, F):
+    plan = _up_check(T, d, E, k, F, 1, "none", tile_m=256)
     assert plan.info["tile_m"] == 256
 
 
@@ -127,9 +126,8 @@ def test_grouped_gemm_full_parity(T, d, E, k, N, bias):
     _grouped_check(T, d, E, k, N, bias)
 
 
-def test_grouped_gemm_pair_mode(monkeypatch):
-    monkeypatch.setenv("MOE_PAIR", "1")
-    plan = _grouped_check(1000, 128, 2, 1, 400, "none")
+def test_grouped_gemm_pair_mode():
+    plan = _grouped_check(1000, 128, 2, 1, 400, "none", tile_m=256)
     assert plan.info["tile_m"] == 256
 
 
@@ -161,20 +159,19 @@ def test_dispatch_and_grouped_calls_share_a_plan():
 
 # ------------------------------------------------------------------ whole FFN
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_swiglu_ffn_chain(monkeypatch, pair):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_swiglu_ffn_chain(tile_m):
     """route -> dispatch + gated up-projection -> down projection -> combine,
     against the oracle chain with H rounded to bf16 (the oracle's rounding)."""
-    monkeypatch.setenv("MOE_PAIR", pair)
     T, d, E, k, F, R = 600, 256, 4, 2, 256, 2  # d = 256: the down projection may pair too
     wl = workloads.custom("ffn", T, d, E, k, 2 * F, R, "none")
     inp = workloads.make_inputs(wl, seed=13, with_weights=False)
     W1, W2 = workloads.make_ffn_weights(wl, F, seed=13)
-    up = binding.moe_plan(T, d, E, k, 2 * F, num_ranks=R)
+    up = binding.moe_plan(T, d, E, k, 2 * F, num_ranks=R, tile_m=tile_m)
     bu = binding.MoeBuffers(up, "cuda", out="H")
-    down = binding.moe_plan(T, F, E, k, d)
+    down = binding.moe_plan(T, F, E, k, d, tile_m=tile_m)
     bd = binding.MoeBuffers(down, "cuda")
-    assert up.info["tile_m"] == down.info["tile_m"] == (256 if pair == "1" else 128)
+    assert up.info["tile_m"] == down.info["tile_m"] == tile_m
     binding.route(up, inp["logits"].cuda(), bu)
     binding.dispatch_gemm_swiglu(up, inp["x"].cuda(), W1.cuda(), bu)
     binding.moe_grouped_gemm(down, bu.H, bu.offsets, W2.cuda(), bd.Y, bd.workspace, bd.status)
