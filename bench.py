@@ -47,6 +47,7 @@ def _args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--tile-m", type=int, default=0, help="128 (one CTA per tile), 256 (CTA pairs), 0 auto")
     ap.add_argument("--producer-ctas", type=int, default=0)
     ap.add_argument("--ffn", choices=["auto", "on", "off"], default="auto",
                     help="also time the gated (SwiGLU) expert FFN with F = N (auto: Mixtral-shaped only)")
@@ -334,7 +335,7 @@ def run_ours(args, wl):
     x = inp["x"].to(dev)
     W = inp["W"]
     logits = inp["logits"].to(dev)
-    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n,
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n, tile_m=args.tile_m,
                             producer_ctas=args.producer_ctas, device=local)
     bufs = binding.MoeBuffers(plan, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -422,7 +423,7 @@ def run_ours(args, wl):
     binding.dispatch_gemm(plan, x, W, bufs, stream)  # leave Y as the path computes it
 
     # the fused kernel with a bf16 Y (MOE_OUT_BF16), timed on its own
-    plan_b = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n,
+    plan_b = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n, tile_m=args.tile_m,
                               producer_ctas=args.producer_ctas, out_dtype=binding.MOE_OUT_BF16,
                               device=local)
     bufs_b = binding.MoeBuffers(plan_b, dev)
