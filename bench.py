@@ -406,6 +406,30 @@ def run_ours(args, wl):
     router_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in rev)
     del L_gpu
 
+    # the same step captured once in a CUDA graph and replayed (launch overhead removed)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        binding.forward(plan, logits, x, W, bufs)
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        binding.forward(plan, logits, x, W, bufs)
+    for _ in range(3):
+        graph.replay()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for a_, b_ in gev:
+        flush.fill_(1.0)
+        a_.record(stream)
+        graph.replay()
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"device status after the graph timing: {st}")
+    graph_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in gev)
+    del graph
+
     # the direct-gather variant of the fused kernel (no receive buffers), timed on its own
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
     for _ in range(3):
@@ -525,6 +549,9 @@ def run_ours(args, wl):
                     "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
                     "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,
                     "note": "moe_combine (step after the path), timed separately; not in value"},
+        "cuda_graph": {"step_ms": graph_ms, "eager_step_ms": statistics.median(step_ms),
+                       "note": "route + fused kernel captured in one CUDA graph and replayed; "
+                               "20 replays, L2 flushed; not in value"},
         "direct_gather": {"ms": gather_ms, "tflops": flops / (gather_ms * 1e9),
                           "dispatch_gemm_ms": statistics.median(dg_ms),
                           "speedup_vs_dispatch": statistics.median(dg_ms) / gather_ms,
