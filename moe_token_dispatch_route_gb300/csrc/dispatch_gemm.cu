@@ -473,31 +473,6 @@ __device__ __forceinline__ void store_block_rows(float* tile, const uint32_t (&v
     __syncwarp();
 }
 
-// bf16 epilogue of one 32-column block: each lane holds one row as 16 packed
-// bf16 pairs (low half = the even column); the row's 64 bytes go through the
-// padded shared-memory tile, so every store instruction writes 8 rows x 64 B.
-// With the stride of 36 words the 8 lanes of each 16-byte access phase hit
-// distinct banks, writing and reading.
-__device__ __forceinline__ void store_block_rows_bf16(float* tile_f, const uint32_t (&w)[16],
-                                                      uint16_t* base, size_t ld, int rows_valid,
-                                                      int cols_valid, int lane) {
-    uint32_t* tile = reinterpret_cast<uint32_t*>(tile_f);
-    uint4* mine = reinterpret_cast<uint4*>(tile + lane * kEpiStride);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mine[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-    __syncwarp();
-    const int sub = lane & 7;     // row within a group of 8
-    const int chunk = lane >> 3;  // 8-column chunk of the 32
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int row = 8 * j + sub;
-        if (row < rows_valid && 8 * chunk < cols_valid)
-            *reinterpret_cast<uint4*>(base + (size_t)row * ld + 8 * chunk) =
-                *reinterpret_cast<const uint4*>(tile + row * kEpiStride + 4 * chunk);
-    }
-    __syncwarp();
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x = lo: the lower address
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -509,7 +484,9 @@ __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.f + ex
 
 // Epilogue of one accumulator (single or pair tile, `bn` columns) for one warp's
 // 32-row lane quarter: Y in fp32 or bf16, or in gated mode H = silu(gate) * up in
-// bf16 from the gate columns [0, bn/2) and the up columns [bn/2, bn).
+// bf16 from the gate columns [0, bn/2) and the up columns [bn/2, bn).  bf16 output
+// goes 64 columns at a time, packed into 32 words per row, so that it leaves
+// through the same full-line (128-byte) row stores as a 32-column fp32 block.
 __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const TileInfo& ti, int bn,
                                               uint32_t tbase, int q, int lane, float* epi) {
     const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
@@ -517,32 +494,41 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
         const int half = bn / 2;
         const int fcols = min(half, p.F - ti.n * half);
         uint16_t* hbase = p.H + (size_t)(ti.row0 + 32 * q) * p.F + (size_t)ti.n * half;
-        for (int c = 0; c < fcols; c += 32) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32(tbase + (uint32_t)c, g);
-            tmem_ld_32x32(tbase + (uint32_t)(half + c), u);
-            tmem_ld_wait(g);
-            tmem_ld_wait(u);
-            uint32_t w[16];
+        for (int c = 0; c < fcols; c += 64) {
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                w[i] = pack_bf16x2(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                                   swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+            for (int h = 0; h < 2; ++h) {
+                uint32_t g[32], u[32];
+                tmem_ld_32x32(tbase + (uint32_t)(c + 32 * h), g);
+                tmem_ld_32x32(tbase + (uint32_t)(half + c + 32 * h), u);
+                tmem_ld_wait(g);
+                tmem_ld_wait(u);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[16 * h + i] = pack_bf16x2(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                                swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+            }
             if (rows_valid > 0)
-                store_block_rows_bf16(epi, w, hbase + c, (size_t)p.F, rows_valid, fcols - c, lane);
+                store_block_rows(epi, w, reinterpret_cast<float*>(hbase + c), (size_t)p.F / 2, rows_valid,
+                                 (fcols - c) / 2, lane);
         }
     } else if (p.out_bf16) {
         uint16_t* ybase = static_cast<uint16_t*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
         const int ncols = min(bn, p.N - ti.n * bn);
-        for (int c = 0; c < ncols; c += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32(tbase + (uint32_t)c, v);
-            tmem_ld_wait(v);
-            uint32_t w[16];
+        for (int c = 0; c < ncols; c += 64) {
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v[32];
+                tmem_ld_32x32(tbase + (uint32_t)(c + 32 * h), v);
+                tmem_ld_wait(v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[16 * h + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            }
             if (rows_valid > 0)
-                store_block_rows_bf16(epi, w, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
+                store_block_rows(epi, w, reinterpret_cast<float*>(ybase + c), (size_t)p.N / 2, rows_valid,
+                                 (ncols - c) / 2, lane);
         }
     } else {
         float* ybase = static_cast<float*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
