@@ -10,10 +10,10 @@
 // On one GB300 the all-to-all becomes a scatter into R per-rank receive
 // buffers in local HBM.  Design:
 //  * Grid = one CTA per SM (about 200 KB of shared memory each, so exactly one
-//    fits), 256 threads.  Each CTA takes a ticket from a workspace counter
-//    when it starts; the first `producer_ctas` tickets take the scatter role
-//    first.  Only CTAs that are running take tickets, so a GEMM CTA never
-//    waits for a scatter CTA that has not been scheduled.
+//    fits), 256 threads, all resident together as in any persistent kernel.
+//    Each CTA takes a ticket from a workspace counter when it starts; the
+//    first `producer_ctas` tickets (by default all of them) take the scatter
+//    role first.
 //  * Scatter role: all 8 warps copy destination rows (perm -> token row of x)
 //    into the rank buffers with 16-byte loads and stores, 4 rows per work
 //    unit, in the order the GEMM consumes them.  The last unit of each
@@ -28,6 +28,10 @@
 //    TMEM, two accumulators so the epilogue of one tile overlaps the next
 //    tile's MMAs); warps 4-7 read the accumulator with tcgen05.ld and store
 //    the valid rows and columns of Y (fp32) with streaming stores.
+//  * Variants of the same kernel: a gated (SwiGLU) epilogue that writes
+//    silu(gate) * up in bf16 from the two halves of a tile; a bf16 Y; a
+//    grouped mode on rows already in place (no scatter, no flags); and a
+//    direct-gather mode whose warps 2-3 copy A rows straight from x.
 //  * Every wait is bounded (globaltimer).  A ready flag that never comes is
 //    reported as MOE_ERR_TIMEOUT and the tile is computed anyway, so the
 //    pipeline stays consistent; a pipeline wait that gives up reports
