@@ -253,3 +253,18 @@ def test_bf16_output_mixtral_full_size_sampled():
         for j in range(len(cols)):
             want[i, j] = oracle.gemm_entry(a_rows[i], cache[e], j)
     _check_bf16(got, want)
+
+
+def test_empty_batch_every_gemm_entry_point():
+    """T = 0: every GEMM entry point returns MOE_OK without launching, and the
+    outputs (all zero-sized) need no pointers."""
+    plan = binding.moe_plan(0, 128, 8, 2, 256)
+    ws = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device="cuda")
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    W = torch.zeros(8, 128, 256, dtype=torch.bfloat16, device="cuda")
+    binding.moe_dispatch_gemm(plan, None, None, None, W, [], None, ws, st)
+    binding.moe_gather_gemm(plan, None, None, None, W, None, ws, st)
+    binding.moe_grouped_gemm(plan, None, None, W, None, ws, st)
+    binding.moe_dispatch_gemm_swiglu(plan, None, None, None, W, [], None, ws, st)
+    rc, status = binding.moe_read_status(st)
+    assert rc == 0 and status == [0, 0, 0, 0]
