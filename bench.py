@@ -406,6 +406,27 @@ def run_ours(args, wl):
     router_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in rev)
     del L_gpu
 
+    # one traced launch: where the fused kernel's time goes, per CTA (moe_set_trace)
+    trace = torch.zeros(plan.info["sm_count"] * binding.TRACE_WORDS, dtype=torch.int64, device=dev)
+    binding.moe_set_trace(plan, trace)
+    flush.fill_(2.0)
+    binding.dispatch_gemm(plan, x, W, bufs, stream)
+    torch.cuda.synchronize(dev)
+    binding.moe_set_trace(plan, None)
+    tr = trace.view(-1, binding.TRACE_WORDS)[: plan.info["num_ctas"]].cpu().double()
+    fi = {n: i for i, n in enumerate(binding.TRACE_FIELDS)}
+    t0 = tr[:, fi["start"]].min()
+    us = lambda col: ((tr[:, fi[col]] - t0) / 1e3)
+    trace_info = {
+        "scatter_end_us": [float(us("scatter_end").median()), float(us("scatter_end").max())],
+        "first_tile_us": [float(us("first_tile").median()), float(us("first_tile").max())],
+        "flag_wait_us": [float(tr[:, fi["flag_wait_ns"]].median() / 1e3), float(tr[:, fi["flag_wait_ns"]].max() / 1e3)],
+        "end_us": [float(us("end").median()), float(us("end").max())],
+        "note": "one traced launch of the fused kernel, per-CTA global-timer stamps from the first CTA's "
+                "start: [median, max] over CTAs",
+    }
+    del trace
+
     # the same step captured once in a CUDA graph and replayed (launch overhead removed)
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -549,6 +570,7 @@ def run_ours(args, wl):
                     "gbs": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6),
                     "frac_hbm": (wl.S * wl.N * 4 + wl.T * wl.N * 4) / (combine_ms * 1e6) / hbm_peak,
                     "note": "moe_combine (step after the path), timed separately; not in value"},
+        "trace": trace_info,
         "cuda_graph": {"step_ms": graph_ms, "eager_step_ms": statistics.median(step_ms),
                        "note": "route + fused kernel captured in one CUDA graph and replayed; "
                                "20 replays, L2 flushed; not in value"},

@@ -276,6 +276,22 @@ MOE_API moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const 
                                       int32_t* dev_status, void* stream);
 
 /*
+ * moe_set_trace -- per-CTA timing records of the plan's later GEMM launches
+ * (moe_dispatch_gemm and its variants), for measuring the schedule: where a
+ * launch's time goes between the scatter, the ready-flag waits and the GEMM.
+ *   trace  in/out: device buffer of at least (SM count) x 8 uint64 (the SM count
+ *                  is moe_plan_info's sm_count), 8-byte aligned; NULL turns
+ *                  tracing off (the default).  Each launch overwrites record b
+ *                  (words 8b .. 8b+7) of every CTA b it runs:
+ *                  0 start, 1 end of its scatter share (0 if none), 2 first
+ *                  tile's rows ready, 4 tiles it loaded, 5 last load issued,
+ *                  6 end (global-timer ns); 3 total ns waiting for ready flags;
+ *                  7 its role ticket.
+ * The records cost a few stores per tile.  Host only; no launch.
+ */
+MOE_API moe_status_t moe_set_trace(moe_plan_t plan, void* trace, int64_t bytes);
+
+/*
  * moe_router_logits -- the step before the path: the router logits that
  * moe_route consumes, L = x @ W_r + bias, on the GPU.  The articles name no
  * router; this library fixes its arithmetic so that routing stays bit-exact

@@ -67,7 +67,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
             "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
             "moe_router_logits", "moe_route_biased", "moe_dispatch_gemm_swiglu",
-            "moe_grouped_gemm", "moe_gather_gemm")
+            "moe_grouped_gemm", "moe_gather_gemm", "moe_set_trace")
 
 
 def load_library(path: str = LIB_PATH):
@@ -97,6 +97,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm_swiglu.restype = I32
     lib.moe_grouped_gemm.argtypes = [VP] * 8
     lib.moe_gather_gemm.argtypes = [VP] * 9
+    lib.moe_set_trace.argtypes = [VP, VP, ctypes.c_int64]
+    lib.moe_set_trace.restype = I32
     lib.moe_gather_gemm.restype = I32
     lib.moe_grouped_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
@@ -235,6 +237,17 @@ def moe_gather_gemm(plan: Plan, x, offsets, perm, W, Y, workspace, dev_status, s
 
 def gather_gemm(plan: Plan, x, W, bufs: "MoeBuffers", stream=None):
     moe_gather_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.Y, bufs.workspace, bufs.status, stream)
+
+
+TRACE_WORDS = 8
+TRACE_FIELDS = ("start", "scatter_end", "first_tile", "flag_wait_ns", "tiles", "issue_end", "end", "role")
+
+
+def moe_set_trace(plan: Plan, trace) -> None:
+    """Per-CTA timing records of later GEMM launches into `trace` (a device int64
+    tensor of at least sm_count * 8 words), or None to stop."""
+    nbytes = 0 if trace is None else trace.numel() * trace.element_size()
+    _check(load_library().moe_set_trace(plan.handle, _ptr(trace), nbytes), "moe_set_trace")
 
 
 def moe_router_logits(plan: Plan, x, W_r, bias, logits, stream=None) -> None:

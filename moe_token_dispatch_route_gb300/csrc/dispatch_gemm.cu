@@ -96,6 +96,15 @@ struct Waiter {
     uint32_t epoch;
 };
 
+// Trace stamps (moe_set_trace): one record of kTraceWords per CTA, written by
+// one thread each; nothing is written when the trace is off.
+__device__ __forceinline__ void trace_set(const DispatchGemmParams& p, int word, unsigned long long v) {
+    if (p.trace) p.trace[(size_t)blockIdx.x * kTraceWords + word] = v;
+}
+__device__ __forceinline__ void trace_add(const DispatchGemmParams& p, int word, unsigned long long v) {
+    if (p.trace) p.trace[(size_t)blockIdx.x * kTraceWords + word] += v;
+}
+
 // Bounded mbarrier wait.  Returns false if the CTA is aborting or the wait
 // exceeded the timeout (then it reports MOE_ERR_DEVICE and starts the abort).
 __device__ bool wait_bar(uint32_t bar, uint32_t parity, const Waiter& w, int where,
@@ -643,8 +652,19 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     TileInfo cur;
     uint32_t cur_flag = 0;
     bool ok = push_next(cur, cur_flag);
+    bool first = true;
     while (ok && cur.rows >= 0) {
-        if (cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+        if (p.trace) {
+            const unsigned long long t0 = global_timer_ns();
+            if (cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+            const unsigned long long t1 = global_timer_ns();
+            trace_add(p, kTrFlagWait, t1 - t0);
+            trace_add(p, kTrTiles, 1);
+            if (first) trace_set(p, kTrFirstTile, t1);
+            first = false;
+        } else if (cur_flag != w.epoch) {
+            wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+        }
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
@@ -680,6 +700,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         cur = nxt;
         cur_flag = nxt_flag;
     }
+    if (p.trace) trace_set(p, kTrIssueEnd, global_timer_ns());
     // no TMA write may still be landing in shared memory when the CTA exits
 #pragma unroll
     for (int s = 0; s < STAGES; ++s)
@@ -936,6 +957,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const uint32_t epoch = ctl->epoch;
     const int role = ctl->role;
+    if (tid == 0 && p.trace) {  // the same thread runs the TMA role: no other writer yet
+        for (int i = 0; i < kTraceWords; ++i) trace_set(p, i, 0ull);
+        trace_set(p, kTrStart, global_timer_ns());
+        trace_set(p, kTrRole, (unsigned long long)role);
+    }
 
     const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
     const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
@@ -944,7 +970,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
         scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl, C::kScatterSlots);
         __syncthreads();
-        if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
+        if (tid == 0) {
+            const unsigned long long t = global_timer_ns();
+            atomicMax(w64 + kHdrScatterEnd / 2, t);
+            trace_set(p, kTrScatterEnd, t);
+        }
     }
 
     if (warp == 0) {
@@ -961,6 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && p.trace) trace_set(p, kTrEnd, global_timer_ns());
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
@@ -1108,8 +1139,19 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     uint32_t cur_flag = 0;
     bool got = false;
     bool ok = next_tile(cur, cur_flag, true, got);
+    bool first = true;
     while (ok && cur.e >= 0) {
-        if (cur.rows > 0 && cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+        if (p.trace) {
+            const unsigned long long t0 = global_timer_ns();
+            if (cur.rows > 0 && cur_flag != w.epoch) wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+            const unsigned long long t1 = global_timer_ns();
+            trace_add(p, kTrFlagWait, t1 - t0);
+            trace_add(p, kTrTiles, 1);
+            if (first) trace_set(p, kTrFirstTile, t1);
+            first = false;
+        } else if (cur.rows > 0 && cur_flag != w.epoch) {
+            wait_flag(p.flags + cur.mtile, w, cur.mtile, cur.e);
+        }
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
@@ -1149,6 +1191,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         cur = nxt;
         cur_flag = nxt_flag;
     }
+    if (p.trace) trace_set(p, kTrIssueEnd, global_timer_ns());
     // the leader drains its stage barriers: each one completes only when both CTAs'
     // loads of that stage have landed
     if (leader) {
@@ -1324,6 +1367,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const uint32_t epoch = ctl->epoch;
     const int scatter_index = 2 * ctl->role + (int)(rank & 1u);
+    if (tid == 0 && p.trace) {  // the same thread runs the TMA role: no other writer yet
+        for (int i = 0; i < kTraceWords; ++i) trace_set(p, i, 0ull);
+        trace_set(p, kTrStart, global_timer_ns());
+        trace_set(p, kTrRole, (unsigned long long)ctl->role);
+    }
 
     const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
     const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
@@ -1332,7 +1380,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
         scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl, C::kScatterSlots);
         __syncthreads();
-        if (tid == 0) atomicMax(w64 + kHdrScatterEnd / 2, (unsigned long long)global_timer_ns());
+        if (tid == 0) {
+            const unsigned long long t = global_timer_ns();
+            atomicMax(w64 + kHdrScatterEnd / 2, t);
+            trace_set(p, kTrScatterEnd, t);
+        }
     }
 
     if (warp == 0) {
@@ -1348,6 +1400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && p.trace) trace_set(p, kTrEnd, global_timer_ns());
     cluster_sync_all();  // no CTA leaves while its peer may still signal it
     if (warp == 2) {
         tc_fence_after();

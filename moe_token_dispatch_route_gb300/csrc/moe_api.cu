@@ -30,6 +30,7 @@ struct moe_plan_s {
     int band = 0;
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
     bool single_ready = false;  // pair plans: single-CTA kernel attributes set (direct gather)
+    unsigned long long* trace = nullptr;  // per-CTA trace records (moe_set_trace), or null
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
     bool maps_valid = false;
@@ -396,6 +397,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
         for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
     prm.Y = Y;
     prm.out_bf16 = plan->shape.out_dtype == MOE_OUT_BF16 ? 1 : 0;
+    prm.trace = plan->trace;
     prm.H = H;
     prm.glu = glu ? 1 : 0;
     prm.F = plan->N / 2;
@@ -485,6 +487,17 @@ moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const int32_t*
                               void* stream) {
     return run_gemm(plan, GemmMode::kGrouped, nullptr, offsets, nullptr, W, nullptr, A, Y, nullptr,
                     workspace, dev_status, stream);
+}
+
+moe_status_t moe_set_trace(moe_plan_t plan, void* trace, int64_t bytes) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    if (!trace) {
+        plan->trace = nullptr;
+        return MOE_OK;
+    }
+    if (!aligned(trace, 8) || bytes < (int64_t)plan->sm_count * kTraceWords * 8) return MOE_ERR_INVALID_ARG;
+    plan->trace = static_cast<unsigned long long*>(trace);
+    return MOE_OK;
 }
 
 moe_status_t moe_router_logits(moe_plan_t plan, const uint16_t* x, const uint16_t* W_r,

@@ -101,7 +101,19 @@ struct DispatchGemmParams {
     int gather;                     // 1: A rows are copied from x by perm into shared memory
                                     //    (no receive buffers, no scatter, no flags)
     int out_bf16;                   // 1: Y is bf16 (fp32 accumulator rounded once)
+    unsigned long long* trace;      // [grid][kTraceWords] per-CTA stamps, or null (off)
 };
+
+// Per-CTA trace record (moe_set_trace): global-timer stamps in ns and counters.
+constexpr int kTraceWords = 8;
+constexpr int kTrStart = 0;      // CTA past its setup
+constexpr int kTrScatterEnd = 1; // CTA finished its scatter share (0: no scatter role)
+constexpr int kTrFirstTile = 2;  // TMA thread: first tile's rows ready (after its flag)
+constexpr int kTrFlagWait = 3;   // TMA thread: total ns waiting for ready flags
+constexpr int kTrTiles = 4;      // TMA thread: tiles this CTA loaded (pair tiles count once per CTA)
+constexpr int kTrIssueEnd = 5;   // TMA thread: last load issued
+constexpr int kTrEnd = 6;        // CTA done with its roles
+constexpr int kTrRole = 7;       // role ticket
 
 cudaError_t launch_dispatch_gemm(const DispatchGemmParams& p, int grid, int stages,
                                  size_t smem, cudaStream_t stream);
