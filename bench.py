@@ -49,6 +49,8 @@ def _args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--tile-m", type=int, default=0, help="128 (one CTA per tile), 256 (CTA pairs), 0 auto")
+    ap.add_argument("--l2", choices=["flush", "none"], default="flush",
+                    help="between timed steps: flush L2 (default) or rely on inputs larger than L2")
     ap.add_argument("--producer-ctas", type=int, default=0)
     ap.add_argument("--ffn", choices=["auto", "on", "off"], default="auto",
                     help="also time the gated (SwiGLU) expert FFN with F = N (auto: Mixtral-shaped only)")
@@ -355,7 +357,8 @@ def run_ours(args, wl):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         for i in range(K):
-            flush.fill_(float(i))  # evict L2 between steps (outside the events)
+            if args.l2 == "flush":
+                flush.fill_(float(i))  # evict L2 between steps (outside the events)
             e0, e1, e2 = ev[i]
             e0.record(stream)
             binding.route(plan, logits, bufs, stream)
@@ -575,7 +578,8 @@ def run_ours(args, wl):
         "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**wl.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "l2": (f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)" if args.l2 == "flush"
+                          else f"no flush: inputs larger than L2 (W {wl.E * wl.d * wl.N * 2 >> 20} MiB)"),
                    "tile_m": plan.info["tile_m"], "tile_n": plan.info["tile_n"],
                    "producer_ctas": plan.info["producer_ctas"],
                    "num_ctas": plan.info["num_ctas"], "stages": plan.info["stages"]},
