@@ -268,3 +268,33 @@ def test_empty_batch_every_gemm_entry_point():
     binding.moe_dispatch_gemm_swiglu(plan, None, None, None, W, [], None, ws, st)
     rc, status = binding.moe_read_status(st)
     assert rc == 0 and status == [0, 0, 0, 0]
+
+
+def test_misaligned_pointers_are_refused_before_any_launch():
+    wl = workloads.custom("align", 256, 128, 4, 2, 256)
+    inp = workloads.make_inputs(wl, seed=19)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N)
+    bufs = binding.MoeBuffers(plan, "cuda")
+    x, W = inp["x"].cuda(), inp["W"].cuda()
+    binding.route(plan, inp["logits"].cuda(), bufs)
+    Y_flat = torch.empty(wl.S * wl.N + 4, dtype=torch.float32, device="cuda")
+    with pytest.raises(binding.MoeError) as exc:  # Y 4 bytes past a 16-byte boundary
+        binding.moe_dispatch_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.recv, Y_flat[1:].data_ptr(),
+                                  bufs.workspace, bufs.status)
+    assert exc.value.status == binding.MOE_ERR_INVALID_ARG
+    ws = torch.zeros(plan.workspace_bytes // 4 + 128, dtype=torch.int32, device="cuda")
+    with pytest.raises(binding.MoeError) as exc:  # workspace off its 256-byte alignment
+        binding.moe_dispatch_gemm(plan, x, bufs.offsets, bufs.perm, W, bufs.recv, bufs.Y,
+                                  ws[4:].data_ptr(), bufs.status)
+    assert exc.value.status == binding.MOE_ERR_WORKSPACE
+    x_flat = torch.empty(wl.T * wl.d + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.MoeError) as exc:  # x 2 bytes past a 16-byte boundary
+        binding.moe_gather_gemm(plan, x_flat[1:].data_ptr(), bufs.offsets, bufs.perm, W, bufs.Y,
+                                bufs.workspace, bufs.status)
+    assert exc.value.status == binding.MOE_ERR_INVALID_ARG
+    # nothing ran: the status word is still clean and a correct call still works
+    rc, status = binding.moe_read_status(bufs.status)
+    assert rc == 0, status
+    binding.dispatch_gemm(plan, x, W, bufs)
+    rc, status = binding.moe_read_status(bufs.status)
+    assert rc == 0, status
