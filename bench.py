@@ -420,12 +420,16 @@ def run_ours(args, wl):
     tr = trace.view(-1, binding.TRACE_WORDS)[: plan.info["num_ctas"]].cpu().double()
     fi = {n: i for i, n in enumerate(binding.TRACE_FIELDS)}
     t0 = tr[:, fi["start"]].min()
-    us = lambda col: ((tr[:, fi[col]] - t0) / 1e3)
+    us = lambda col, rows=slice(None): ((tr[rows, fi[col]] - t0) / 1e3)
+    loaded = tr[:, fi["tiles"]] > 0  # CTAs that loaded at least one tile
+    scattered = tr[:, fi["scatter_end"]] > 0
+    med_max = lambda v: [float(v.median()), float(v.max())] if v.numel() else None
     trace_info = {
-        "scatter_end_us": [float(us("scatter_end").median()), float(us("scatter_end").max())],
-        "first_tile_us": [float(us("first_tile").median()), float(us("first_tile").max())],
-        "flag_wait_us": [float(tr[:, fi["flag_wait_ns"]].median() / 1e3), float(tr[:, fi["flag_wait_ns"]].max() / 1e3)],
-        "end_us": [float(us("end").median()), float(us("end").max())],
+        "scatter_end_us": med_max(us("scatter_end", scattered)),
+        "first_tile_us": med_max(us("first_tile", loaded)),
+        "flag_wait_us": med_max(tr[loaded, fi["flag_wait_ns"]] / 1e3),
+        "end_us": med_max(us("end")),
+        "ctas_with_tiles": int(loaded.sum()),
         "note": "one traced launch of the fused kernel, per-CTA global-timer stamps from the first CTA's "
                 "start: [median, max] over CTAs",
     }
