@@ -298,3 +298,39 @@ def test_misaligned_pointers_are_refused_before_any_launch():
     binding.dispatch_gemm(plan, x, W, bufs)
     rc, status = binding.moe_read_status(bufs.status)
     assert rc == 0, status
+
+
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_calls_with_changing_routing_share_a_workspace(tile_m):
+    """Three calls on one plan and workspace with different tokens and logits,
+    so the experts' row counts (and the tiles whose flags the epoch tags) change
+    from call to call; every call matches the oracle."""
+    wl = workloads.custom("change", 900, 128, 8, 2, 512, 2, "zipf")
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=tile_m)
+    bufs = binding.MoeBuffers(plan, "cuda")
+    W_cpu = workloads.make_weights(wl, seed=30)
+    W = W_cpu.cuda()
+    for seed in (31, 32, 33):
+        inp = workloads.make_inputs(wl, seed=seed, with_weights=False)
+        bufs.Y.fill_(float("nan"))
+        binding.forward(plan, inp["logits"].cuda(), inp["x"].cuda(), W, bufs)
+        rc, status = binding.moe_read_status(bufs.status)
+        assert rc == 0, (seed, status)
+        ref = oracle.route(inp["logits"].numpy(), wl.k)
+        check_route(bufs, ref, wl.k)
+        rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+        check_Y(bufs.Y.cpu().double().numpy(),
+                oracle.grouped_gemm(rows, workloads.bf16_bits(W_cpu), ref["offsets"]))
+
+
+def test_receive_capacity_exactly_enough_and_one_short():
+    wl = workloads.custom("capx", 500, 128, 8, 2, 256, 4, "zipf")
+    inp = workloads.make_inputs(wl, seed=34)
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    base = oracle.rank_base(ref["offsets"], wl.R)
+    need = int(np.max(np.diff(base)))
+    plan, bufs, rc, status = run_path(wl, inp, rank_capacity_rows=need)
+    assert rc == 0, status
+    check_recv(bufs, workloads.bf16_bits(inp["x"]), ref, wl.k, wl.R)
+    plan, bufs, rc, status = run_path(wl, inp, rank_capacity_rows=need - 1)
+    assert rc == binding.MOE_ERR_CAPACITY, status
