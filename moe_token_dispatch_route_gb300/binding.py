@@ -96,11 +96,11 @@ def load_library(path: str = LIB_PATH):
     lib.moe_dispatch_gemm_swiglu.argtypes = [VP] * 10
     lib.moe_dispatch_gemm_swiglu.restype = I32
     lib.moe_grouped_gemm.argtypes = [VP] * 8
+    lib.moe_grouped_gemm.restype = I32
     lib.moe_gather_gemm.argtypes = [VP] * 9
+    lib.moe_gather_gemm.restype = I32
     lib.moe_set_trace.argtypes = [VP, VP, ctypes.c_int64]
     lib.moe_set_trace.restype = I32
-    lib.moe_gather_gemm.restype = I32
-    lib.moe_grouped_gemm.restype = I32
     lib.moe_read_status.argtypes = [VP, VP, P(I32)]
     lib.moe_read_status.restype = I32
     lib.moe_router_logits.argtypes = [VP] * 6
