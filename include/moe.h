@@ -60,7 +60,7 @@ extern "C" {
 typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad field   */
-    MOE_ERR_UNSUPPORTED = 2,  /* valid arguments outside this build's shape limits    */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid arguments outside the library's shape limits */
     MOE_ERR_WORKSPACE = 3,    /* workspace missing or misaligned                      */
     MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (or no device)     */
     MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait for a ready flag gave up      */
