@@ -44,3 +44,21 @@ def test_finegrained_has_empty_experts_and_skew(oracle_mod):
     assert int(counts.sum()) == w.S
     srt = np.sort(counts)[::-1]
     assert srt[0] > 4 * np.median(counts)   # skewed, not uniform
+
+
+def test_ffn_weights_and_prelaid_rows_are_seeded_and_scaled():
+    w = wl.custom("ffn", 64, 256, 4, 2, 96)
+    W1, W2 = wl.make_ffn_weights(w, 96, seed=3)
+    W1b, W2b = wl.make_ffn_weights(w, 96, seed=3)
+    assert W1.shape == (4, 256, 192) and W2.shape == (4, 96, 256)
+    assert W1.dtype == W2.dtype == torch.bfloat16
+    assert torch.equal(W1, W1b) and torch.equal(W2, W2b)
+    assert not torch.equal(W1[:, :, :96], W1[:, :, 96:])  # gate and up halves differ
+    # N(0, 1/d) and N(0, 1/F)
+    assert abs(float(W1.float().std()) * 256 ** 0.5 - 1.0) < 0.05
+    assert abs(float(W2.float().std()) * 96 ** 0.5 - 1.0) < 0.05
+    A = wl.make_rows(1500, 128, seed=3)
+    assert A.shape == (1500, 128) and A.dtype == torch.bfloat16
+    assert torch.equal(A, wl.make_rows(1500, 128, seed=3))
+    assert abs(float(A.float().std()) - 0.5) < 0.02
+    assert wl.make_rows(0, 128).shape == (0, 128)
