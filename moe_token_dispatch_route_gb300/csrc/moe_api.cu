@@ -224,7 +224,7 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->producer_ctas = std::max(1, std::min(p->producer_ctas, p->num_ctas));
     if (p->pair) p->producer_ctas = std::min(p->num_ctas, (p->producer_ctas + 1) & ~1);  // whole pairs
     p->max_mtiles = (int)(p->S / kTileM) + p->E;
-    p->route_blocks = route_blocks_for(p->T, sms);
+    p->route_blocks = route_blocks_for(p->T, p->E, sms);
     p->timeout_ns = shape->timeout_ns != 0 ? shape->timeout_ns : kDefaultTimeoutNs;
     p->skip_publish = shape->debug_skip_publish > 0 ? shape->debug_skip_publish - 1 : -1;
     // tuning override for sweeps only: row tiles per schedule band (0 = whole expert)

@@ -69,9 +69,11 @@ struct RouteArgs {
     int sigmoid;      // 1: gate score = logistic(logit); 0: softmax over all E
 };
 
-// Routing CTAs for T tokens: tokens per CTA is the smallest of 8, 16, 32, 64 that
-// keeps the CTA count within the SM count (64 when none does).
-int route_blocks_for(int T, int sm_count);
+// Routing CTAs for T tokens and E experts: tokens per CTA is the smallest of 8, 16,
+// 32, 64 that keeps the CTA count within max(SM count, kRouteScanEntries / E) (64
+// when none does).
+constexpr int kRouteScanEntries = 16384;
+int route_blocks_for(int T, int E, int sm_count);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t route_prepare_attributes();
 

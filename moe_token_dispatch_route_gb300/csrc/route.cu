@@ -312,9 +312,13 @@ cudaError_t launch_select(const RouteArgs& a, cudaStream_t stream) {
 
 cudaError_t route_prepare_attributes() { return cudaSuccess; }  // < 48 KB dynamic smem
 
-int route_blocks_for(int T, int sm_count) {
+int route_blocks_for(int T, int E, int sm_count) {
+    // As many CTAs as keep the last CTA's scan over the [CTAs][E] count table near
+    // 64 loads per thread, and at least one per SM: with few experts that means one
+    // token per warp (no serial token loop), with many a few tokens per warp.
+    const int max_blocks = std::max(sm_count, kRouteScanEntries / std::max(1, E));
     int chunk = 8;
-    while (chunk < kRouteChunk && (T + chunk - 1) / chunk > sm_count) chunk *= 2;
+    while (chunk < kRouteChunk && (T + chunk - 1) / chunk > max_blocks) chunk *= 2;
     return (T + chunk - 1) / chunk;
 }
 
