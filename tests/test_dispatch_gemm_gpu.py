@@ -198,6 +198,7 @@ def test_pair_mode_missing_flag_times_out():
 @pytest.mark.parametrize("T,d,E,k,N,R", [
     (1024, 128, 1024, 8, 64, 32),   # the largest E and R the library accepts
     (200, 64, 64, 32, 32, 4),       # the largest k
+    (130, 65536, 1, 1, 16, 1),      # the largest d: 1024 k-blocks per tile
 ])
 def test_limits_full_parity(T, d, E, k, N, R):
     _full_check(workloads.custom("limits", T, d, E, k, N, R))
