@@ -72,7 +72,7 @@ struct RouteArgs {
 // Routing CTAs for T tokens and E experts: tokens per CTA is the smallest of 8, 16,
 // 32, 64 that keeps the CTA count within max(SM count, kRouteScanEntries / E) (64
 // when none does).
-constexpr int kRouteScanEntries = 16384;
+constexpr int kRouteScanEntries = 4096;
 int route_blocks_for(int T, int E, int sm_count);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 cudaError_t route_prepare_attributes();

@@ -11,8 +11,10 @@
 // Two launches, no atomics that decide an order:
 //  1. route_select_kernel: one CTA per 8-64 tokens, one warp per token at a
 //     time.  Each warp holds its token's E logits in registers (E/32 per
-//     lane), reduces max and sum-of-exp with xor shuffles and runs k rounds
-//     of a warp arg-max.  The CTA records which of its tokens picked each
+//     lane), takes their maximum with a warp max over order-preserving
+//     integer keys and their sum of exponentials with xor shuffles, and runs
+//     k rounds of a warp arg-max (a warp max of the keys, then a warp min of
+//     the expert indices that hold it).  The CTA records which of its tokens picked each
 //     expert as a bit mask (one bit per token), from which the per-CTA
 //     count and every slot's rank inside the CTA follow by popcount.  The
 //     last CTA to finish (ticket counter) turns the per-CTA counts into the
@@ -88,9 +90,13 @@ cudaError_t launch_select(const RouteArgs& a, cudaStream_t stream) {
 cudaError_t route_prepare_attributes() { return cudaSuccess; }  // < 48 KB dynamic smem
 
 int route_blocks_for(int T, int E, int sm_count) {
-    // As many CTAs as keep the last CTA's scan over the [CTAs][E] count table near
-    // 64 loads per thread, and at least one per SM: with few experts that means one
-    // token per warp (no serial token loop), with many a few tokens per warp.
+    // As many CTAs as keep the last CTA's scan over the [CTAs][E] count table at
+    // about 16 loads per thread (one round of loads in flight), and at least one
+    // per SM.  A sweep of 8-64 tokens per CTA on one GB300 (graph replays, L2
+    // flushed) found the scan's length the limit beyond that: on the
+    // Mixtral-shaped batch (8192 tokens, 8 experts) 512 CTAs of 16 tokens route
+    // in 13.0 us, 1024 CTAs of 8 in 16.4 us; on the fine-grained one (16384
+    // tokens, 64 experts) 2048 CTAs of 8 take 82 us, 256 of 64 take 28 us.
     const int max_blocks = std::max(sm_count, kRouteScanEntries / std::max(1, E));
     int chunk = 8;
     while (chunk < kRouteChunk && (T + chunk - 1) / chunk > max_blocks) chunk *= 2;

@@ -1,5 +1,4 @@
-// Device code of the routing step, shared by the routing kernels (route.cu)
-// and the fused forward kernel (dispatch_gemm.cu): per-chunk top-k, histogram
+// Device code of the routing kernels (route.cu): per-chunk top-k, histogram
 // and ranks, and the scan that turns per-chunk counts into offsets and bases.
 // Each file that includes it gets its own copy (internal linkage).
 #pragma once
@@ -15,10 +14,16 @@ namespace {
 constexpr unsigned kRouteFull = 0xFFFFFFFFu;
 constexpr int kMaskWords = kRouteChunk / 32;  // bit-mask words per expert
 
-// (v1, e1) ranks before (v2, e2): larger logit first, lower index between equals.
-// Float == treats -0.0 and +0.0 as equal, so the index decides there.
-__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
-    return v1 > v2 || (v1 == v2 && e1 < e2);
+// Order-preserving key of a finite float: a larger float has a larger key,
+// equal floats have equal keys (-0.0 is keyed as +0.0), and every key is above
+// 0, which stands for "nothing".  key_value inverts it (zeros come back as +0.0).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Exclusive scan of n <= 1024 ints held in smem `vals`, in place, by 256 threads;
@@ -69,15 +74,13 @@ __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) 
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int s = 0;
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {  // eight independent loads in flight
-            int v[8];
+        for (int b = b0; b < b1; b += 16) {  // sixteen independent loads in flight
+            int v[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(a.blk + (size_t)(b + u) * E + e);
+            for (int u = 0; u < 16; ++u) v[u] = b + u < b1 ? __ldcg(a.blk + (size_t)(b + u) * E + e) : 0;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) s += v[u];
+            for (int u = 0; u < 16; ++u) s += v[u];
         }
-        for (; b < b1; ++b) s += __ldcg(a.blk + (size_t)b * E + e);
         part[job] = s;
     }
     __syncthreads();
@@ -103,22 +106,15 @@ __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) 
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int run = tot[e] + part[job];
-        int b = b0;
-        for (; b + 8 <= b1; b += 8) {
-            int v[8];
+        for (int b = b0; b < b1; b += 16) {
+            int v[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(a.blk + (size_t)(b + u) * E + e);
+            for (int u = 0; u < 16; ++u) v[u] = b + u < b1 ? __ldcg(a.blk + (size_t)(b + u) * E + e) : 0;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                a.blk[(size_t)(b + u) * E + e] = run;
+            for (int u = 0; u < 16; ++u) {
+                if (b + u < b1) a.blk[(size_t)(b + u) * E + e] = run;
                 run += v[u];
             }
-        }
-        for (; b < b1; ++b) {
-            int* p = a.blk + (size_t)b * E + e;
-            const int c = __ldcg(p);
-            *p = run;
-            run += c;
         }
     }
     if (tid == 0) a.hdr[kHdrRouteTicket] = 0;  // ready for the next call
@@ -157,13 +153,13 @@ __device__ void select_chunk(const RouteArgs& a, int c, uint32_t* smem) {
             }
         }
         // softmax statistics over all E logits (unused by the logistic score)
-        float m = -INFINITY, s = 0.f;
+        float m = 0.f, s = 0.f;
         if (!a.sigmoid) {
+            uint32_t mk = 0u;  // the maximum as a warp max of order keys (exact)
 #pragma unroll
             for (int i = 0; i < VPL; ++i)
-                if (live >> i & 1u) m = fmaxf(m, v[i]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kRouteFull, m, off));
+                if (live >> i & 1u) mk = max(mk, order_key(v[i]));
+            m = key_value(__reduce_max_sync(kRouteFull, mk));
 #pragma unroll
             for (int i = 0; i < VPL; ++i)
                 if (live >> i & 1u) s += expf(v[i] - m);
@@ -177,33 +173,29 @@ __device__ void select_chunk(const RouteArgs& a, int c, uint32_t* smem) {
                 if (live >> i & 1u) v[i] += __ldg(a.sel_bias + lane + 32 * i);
         }
 
+        // k rounds of a warp arg-max on the selection keys: the largest key by a
+        // warp max, then the lowest expert index holding it by a warp min
+        uint32_t key[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) key[i] = order_key(v[i]);
         int my_e = -1;
-        float my_v = 0.f;  // the pick's key; equal to its logit when there is no bias
+        float my_v = 0.f;  // the pick's key value; equal to its logit when there is no bias
         for (int j = 0; j < k; ++j) {
-            float bv = 0.f;
-            int be = INT_MAX;  // INT_MAX: nothing left in this lane
+            uint32_t bk = 0u;
+            int bi = -1;  // the lane's best live value: its largest key, lowest i between equals
 #pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                if (live >> i & 1u) {
-                    if (be == INT_MAX || v[i] > bv) {  // strict: lower index kept between equals
-                        bv = v[i];
-                        be = lane + 32 * i;
-                    }
+            for (int i = 0; i < VPL; ++i)
+                if ((live >> i & 1u) && key[i] > bk) {
+                    bk = key[i];
+                    bi = i;
                 }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(kRouteFull, bv, off);
-                const int oe = __shfl_xor_sync(kRouteFull, be, off);
-                if (oe != INT_MAX && (be == INT_MAX || ranks_before(ov, oe, bv, be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) live &= ~(1u << (be >> 5));
+            const uint32_t wk = __reduce_max_sync(kRouteFull, bk);
+            const uint32_t we = __reduce_min_sync(
+                kRouteFull, (bi >= 0 && bk == wk) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+            if (we != 0xFFFFFFFFu && (int)(we & 31u) == lane) live &= ~(1u << (we >> 5));
             if (lane == j) {
-                my_e = be;
-                my_v = bv;
+                my_e = we != 0xFFFFFFFFu ? (int)we : -1;
+                my_v = key_value(wk);
             }
         }
         float my_w = 0.f;
