@@ -49,6 +49,23 @@ def test_route_edge_shapes_with_ties(T, E, k):
     check_route(bufs, oracle.route(L, k), k)
 
 
+@pytest.mark.parametrize("flags", [0, binding.MOE_ROUTE_RENORM])
+@pytest.mark.parametrize("T,E,k", [(500, 8, 2), (400, 64, 4), (300, 300, 8)])
+def test_route_extreme_magnitudes_subnormals_and_signed_zeros(T, E, k, flags):
+    """Logits drawn from the extremes of fp32 (largest finite, smallest normal
+    and subnormal, both zeros), with many exact ties: the selection order is
+    the float order with ties to the lower index, and -0.0 ties with +0.0."""
+    big = np.finfo(np.float32).max
+    tiny = np.finfo(np.float32).tiny
+    sub = np.float32(1e-45)
+    pool = np.array([-big, -1e30, -1.5, -tiny, -1e-40, -sub, -0.0, 0.0, sub, 1e-40, tiny, 1.5, 1e30, big],
+                    np.float32)
+    rng = np.random.default_rng(T + E + k + flags)
+    L = pool[rng.integers(0, pool.size, (T, E))]
+    bufs = _route_only(T, E, k, L, route_flags=flags)
+    check_route(bufs, oracle.route(L, k, renorm=bool(flags & binding.MOE_ROUTE_RENORM)), k)
+
+
 def test_route_all_tokens_one_expert():
     T, E, k = 500, 16, 1
     L = np.zeros((T, E), np.float32)
