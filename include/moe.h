@@ -86,7 +86,8 @@ typedef struct moe_shape {
     int32_t N;                  /* expert output width                                  */
     int32_t num_ranks;          /* R simulated expert ranks; 0 means 1                  */
     int32_t rank_capacity_rows; /* rows in each rank's receive buffer; 0 means T*k      */
-    int32_t tile_n;             /* GEMM tile width: 0 = auto, else 128, 192 or 256      */
+    int32_t tile_n;             /* GEMM tile width: 0 = auto, else 128, 192 or 256;
+                                   512 with CTA pairs only (tile_m 0 or 256, N >= 512)  */
     int32_t producer_ctas;      /* CTAs that start in the scatter role: 0 = all of them */
     int32_t num_ctas;           /* persistent grid size: 0 = one CTA per SM             */
     int64_t timeout_ns;         /* limit of every device-side wait: 0 = 2 s             */

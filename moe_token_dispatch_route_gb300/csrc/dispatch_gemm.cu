@@ -1033,14 +1033,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * Each CTA waits for the ready flag of its own 128-row half.
 // The scatter role is unchanged; a pair takes one role ticket and its two
 // CTAs become scatter CTAs 2t and 2t+1.
-template <int STAGES>
+template <int STAGES, int BN>
 struct PairCfg {
+    static_assert(BN == 256 || BN == 512, "pair tile widths: 256 or 512 columns");
     static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB: this CTA's 128 rows
-    static constexpr int kBBytes = 128 * kTileK * 2;     // 16 KB: this CTA's 128 columns
+    static constexpr int kBN = BN;                       // tile width of the pair
+    static constexpr int kHalves = BN / 256;             // N=256 MMAs per K step
+    static constexpr int kBBytes = (BN / 2) * kTileK * 2;  // this CTA's BN/2 columns: 16 or 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kBN = 256;                      // tile width of the pair
-    static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, kBN);
-    static constexpr int kTmemCols = 2 * kBN;            // two accumulators
+    static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 256);
+    static constexpr int kTmemCols = 512;                // two 256-column accumulators or one of 512
+    static constexpr int kAccs = 512 / BN;               // accumulators (TMEM double buffer for 256)
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 3 * sizeof(int) * (kMaxE + 1);
     static_assert(STAGES <= kMaxStages, "stages");
@@ -1068,11 +1071,11 @@ __device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, 
     ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
 }
 
-template <int STAGES>
+template <int STAGES, int BN>
 __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
                               const int* pt_base, uint8_t* sA, uint8_t* sB, const Waiter& w,
                               bool leader, uint32_t peer) {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, BN>;
     const uint32_t total_tiles = (uint32_t)pt_base[p.E] * (uint32_t)p.n_tiles;
     tma_prefetch_map(&p.b_map);
     for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
@@ -1155,8 +1158,13 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
-        // this CTA's 128 of the pair tile's 256 B columns: boxes 0-1 (leader) or 2-3
-        const int ncol = b_box_col(p, cur.n, C::kBN, leader ? 0 : 2);
+        // this CTA's half of each 256-column MMA: 64-column boxes 4h + {0, 1} (leader) or
+        // 4h + {2, 3} (peer) of the tile, for h < kHalves; box b lands at 8192 b in sB
+        int bcol[2 * C::kHalves];
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, cur.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -1177,9 +1185,10 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
             if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
             tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
-            tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes), &p.b_map, fb, ncol, brow + kb * kTileK);
-            tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192), &p.b_map, fb, ncol + 64,
-                             brow + kb * kTileK);
+#pragma unroll
+            for (int b = 0; b < 2 * C::kHalves; ++b)
+                tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                 brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -1202,10 +1211,10 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     }
 }
 
-template <int STAGES>
+template <int STAGES, int BN>
 __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, uint8_t* sB,
                               uint32_t tmem_base, const Waiter& w) {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, BN>;
     int stage = 0;
     uint32_t phase = 0;
     int slot = 0;
@@ -1236,8 +1245,11 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
 #pragma unroll
             for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
                 const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
+                    const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
+                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                }
             }
             umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
             if (++stage == STAGES) {
@@ -1247,17 +1259,19 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         }
         if (!ok) break;
         umma_commit_pair_mc(smem_addr(&ctl->tfull[acc]), 0x3);
-        acc ^= 1;
-        if (acc == 0) aphase ^= 1u;
+        if (++acc == C::kAccs) {
+            acc = 0;
+            aphase ^= 1u;
+        }
     }
     umma_commit_pair(smem_addr(&ctl->mma_done));
     wait_bar(smem_addr(&ctl->mma_done), 0u, w, 28, false, true);
 }
 
-template <int STAGES>
+template <int STAGES, int BN>
 __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
                                    const Waiter& w, bool leader, uint32_t lead, float* epi) {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, BN>;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
     int slot = 0;
@@ -1293,15 +1307,17 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
             if (leader) mbar_arrive(te);
             else mbar_arrive_cluster(mapa_shared(te, lead));
         }
-        acc ^= 1;
-        if (acc == 0) aphase ^= 1u;
+        if (++acc == C::kAccs) {
+            acc = 0;
+            aphase ^= 1u;
+        }
     }
 }
 
-template <int STAGES>
+template <int STAGES, int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dispatch_gemm_pair_kernel(const __grid_constant__ DispatchGemmParams p) {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -1388,13 +1404,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     if (warp == 0) {
-        if (lane == 0) pair_tma_role<STAGES>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
+        if (lane == 0) pair_tma_role<STAGES, BN>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && leader) pair_mma_role<STAGES>(p, ctl, sA, sB, tmem_base, w);
+        if (lane == 0 && leader) pair_mma_role<STAGES, BN>(p, ctl, sA, sB, tmem_base, w);
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
-        pair_epilogue_role<STAGES>(p, ctl, tmem_base, w, leader, lead,
+        pair_epilogue_role<STAGES, BN>(p, ctl, tmem_base, w, leader, lead,
                                    epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
     }
 
@@ -1433,22 +1449,33 @@ cudaError_t launch_cfg(const DispatchGemmParams& p, int grid, size_t smem, cudaS
 
 }  // namespace
 
-size_t dispatch_gemm_pair_smem_bytes() { return PairCfg<6>::kSmem; }
+size_t dispatch_gemm_pair_smem_bytes(int tile_n) {
+    return tile_n == 512 ? PairCfg<4, 512>::kSmem : tile_n == 256 ? PairCfg<6, 256>::kSmem : 0;
+}
 
-cudaError_t dispatch_gemm_pair_prepare(size_t smem, int* max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_gemm_pair_kernel<6>,
+template <int STAGES, int BN>
+cudaError_t pair_prepare(size_t smem, int* max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_gemm_pair_kernel<STAGES, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
-    return cudaOccupancyMaxActiveClusters(max_clusters, dispatch_gemm_pair_kernel<6>, &cfg);
+    return cudaOccupancyMaxActiveClusters(max_clusters, dispatch_gemm_pair_kernel<STAGES, BN>, &cfg);
+}
+
+cudaError_t dispatch_gemm_pair_prepare(int tile_n, size_t smem, int* max_clusters) {
+    if (tile_n == 512) return pair_prepare<4, 512>(smem, max_clusters);
+    if (tile_n == 256) return pair_prepare<6, 256>(smem, max_clusters);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dispatch_gemm_pair(const DispatchGemmParams& p, int grid, size_t smem,
                                       cudaStream_t stream) {
-    dispatch_gemm_pair_kernel<6><<<grid, kThreads, smem, stream>>>(p);
+    if (p.tile_n == 512) dispatch_gemm_pair_kernel<4, 512><<<grid, kThreads, smem, stream>>>(p);
+    else if (p.tile_n == 256) dispatch_gemm_pair_kernel<6, 256><<<grid, kThreads, smem, stream>>>(p);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

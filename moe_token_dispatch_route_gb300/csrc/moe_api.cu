@@ -109,9 +109,12 @@ moe_status_t validate_shape(const moe_shape_t& s) {
     if (s.N % 16 != 0) return MOE_ERR_UNSUPPORTED;
     if (R > kMaxRanks || s.E % R != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s.T * s.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-    if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 192 && s.tile_n != 256) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_n != 0 && s.tile_n != 128 && s.tile_n != 192 && s.tile_n != 256 && s.tile_n != 512)
+        return MOE_ERR_UNSUPPORTED;
     if (s.tile_m != 0 && s.tile_m != 128 && s.tile_m != 256) return MOE_ERR_UNSUPPORTED;
-    if (s.tile_m == 256 && (s.N < 256 || (s.tile_n != 0 && s.tile_n != 256))) return MOE_ERR_UNSUPPORTED;
+    if (s.tile_m == 256 && (s.N < 256 || (s.tile_n != 0 && s.tile_n != 256 && s.tile_n != 512)))
+        return MOE_ERR_UNSUPPORTED;
+    if (s.tile_n == 512 && (s.tile_m == 128 || s.N < 512)) return MOE_ERR_UNSUPPORTED;  // pairs only
     return MOE_OK;
 }
 
@@ -183,7 +186,8 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->R = shape->num_ranks == 0 ? 1 : shape->num_ranks;
     p->S = (long long)p->T * p->k;
     p->cap = shape->rank_capacity_rows == 0 ? (int)p->S : shape->rank_capacity_rows;
-    p->tile_n = shape->tile_n != 0 ? shape->tile_n : (p->N >= 256 ? 256 : 128);
+    // single-CTA tile width (512-wide tiles exist for CTA pairs only)
+    p->tile_n = shape->tile_n != 0 && shape->tile_n != 512 ? shape->tile_n : (p->N >= 256 ? 256 : 128);
     p->stages = p->tile_n == 128 ? 6 : 4;
     p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
     if (p->smem == 0 || (int)p->smem > smem_optin) {
@@ -194,26 +198,31 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     // CTA pairs for layers with many rows per expert (on average at least one 256-row
     // tile) and full-width tiles, unless the shape fixes tile_m
     if (shape->tile_m == 0)
-        p->pair = p->S >= 256LL * p->E && p->N >= 256 && (shape->tile_n == 0 || shape->tile_n == 256);
+        p->pair = p->S >= 256LL * p->E && p->N >= 256 &&
+                  (shape->tile_n == 0 || shape->tile_n == 256 || shape->tile_n == 512);
     else
         p->pair = shape->tile_m == 256;
     if (p->pair) {
+        const int pair_tn = shape->tile_n == 512 ? 512 : 256;
         int max_clusters = 0;
-        p->smem = dispatch_gemm_pair_smem_bytes();
+        p->smem = dispatch_gemm_pair_smem_bytes(pair_tn);
         if ((int)p->smem > smem_optin ||
-            dispatch_gemm_pair_prepare(p->smem, &max_clusters) != cudaSuccess || max_clusters < 1) {
+            dispatch_gemm_pair_prepare(pair_tn, p->smem, &max_clusters) != cudaSuccess || max_clusters < 1) {
             cudaGetLastError();
-            if (shape->tile_m == 256) {  // pairs were asked for and cannot run here
+            if (shape->tile_m == 256 || shape->tile_n == 512) {  // pairs were asked for and cannot run here
                 delete p;
                 return MOE_ERR_UNSUPPORTED;
             }
             p->pair = false;  // no co-resident pairs: keep the single-CTA kernel
             p->smem = dispatch_gemm_smem_bytes(p->tile_n, p->stages);
         } else {
-            p->tile_n = 256;
-            p->stages = 6;
+            p->tile_n = pair_tn;
+            p->stages = pair_tn == 512 ? 4 : 6;
             p->num_ctas = 2 * std::min(max_clusters, p->num_ctas / 2);
         }
+    } else if (shape->tile_n == 512) {
+        delete p;
+        return MOE_ERR_UNSUPPORTED;
     }
     // Every CTA starts in the scatter role by default: the scatter then ends soonest and
     // the first tiles' flags come earliest.  Measured against 16-96 scatter CTAs this is

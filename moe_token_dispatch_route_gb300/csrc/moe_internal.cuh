@@ -141,8 +141,8 @@ struct CombineArgs {
 cudaError_t launch_combine(const CombineArgs& a, int sm_count, cudaStream_t stream);
 
 // CTA-pair mode (clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2)
-size_t dispatch_gemm_pair_smem_bytes();
-cudaError_t dispatch_gemm_pair_prepare(size_t smem, int* max_clusters);
+size_t dispatch_gemm_pair_smem_bytes(int tile_n);  // tile_n: 256 or 512
+cudaError_t dispatch_gemm_pair_prepare(int tile_n, size_t smem, int* max_clusters);
 cudaError_t launch_dispatch_gemm_pair(const DispatchGemmParams& p, int grid, size_t smem,
                                       cudaStream_t stream);
 cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem);

@@ -71,6 +71,9 @@ def _plan_rc(lib, **kw):
     (dict(k=0), binding.MOE_ERR_INVALID_ARG),
     (dict(route_flags=4), binding.MOE_ERR_INVALID_ARG),
     (dict(debug_skip_publish=-2), binding.MOE_ERR_INVALID_ARG),
+    (dict(tile_n=512, tile_m=128), binding.MOE_ERR_UNSUPPORTED),   # 512-wide tiles: CTA pairs only
+    (dict(tile_n=512, N=256), binding.MOE_ERR_UNSUPPORTED),
+    (dict(tile_n=384), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=1025, k=2), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=8, k=9), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=64, k=33), binding.MOE_ERR_UNSUPPORTED),

@@ -158,6 +158,49 @@ def test_pair_mode_full_parity(T, d, E, k, N, R, bias):
     assert plan.info["tile_m"] == 256
 
 
+@pytest.mark.parametrize("T,d,E,k,N,R,bias", [
+    (1000, 128, 2, 1, 512, 1, "none"),    # one 512-column tile
+    (1200, 256, 4, 2, 1408, 1, "none"),   # ragged N: the last tile holds 384 of 512 columns
+    (800, 128, 4, 2, 528, 2, "zipf"),     # 528 = 512 + 16: the last tile's boxes lie mostly outside W
+    (130, 64, 1, 1, 1024, 1, "none"),     # one expert of 130 rows: the odd half holds 2 rows
+])
+def test_pair_mode_512_wide_tiles_full_parity_and_bits(T, d, E, k, N, R, bias):
+    """512-column pair tiles (two N=256 MMAs per K step into one 512-column
+    accumulator) against the oracle, and bit for bit against 256-column pair
+    tiles: every output element sees the same MMAs in the same K order."""
+    wl = workloads.custom("pair512", T, d, E, k, N, R, bias)
+    plan, bufs = _full_check(wl, tile_m=256, tile_n=512)
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 512 and plan.info["stages"] == 4
+    plan256, bufs256 = _full_check(wl, tile_m=256, tile_n=256)
+    assert plan256.info["tile_n"] == 256
+    assert torch.equal(bufs.Y, bufs256.Y)
+
+
+def test_pair_mode_512_wide_role_split_and_grid_do_not_change_bits():
+    wl = workloads.custom("p512split", 2500, 128, 4, 2, 1024, 1, "none")
+    inp = workloads.make_inputs(wl, seed=11)
+    outs = []
+    for kw in (dict(), dict(producer_ctas=2), dict(num_ctas=16, producer_ctas=4), dict(num_ctas=2)):
+        _, bufs, rc, status = run_path(wl, inp, tile_m=256, tile_n=512, **kw)
+        assert rc == 0, status
+        outs.append(bufs.Y.clone())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "finegrained"])
+def test_pair_mode_512_wide_full_size(name):
+    wl = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
+    plan, bufs, rc, status = run_path(wl, inp, tile_n=512)
+    assert rc == 0, status
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 512
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    xb = workloads.bf16_bits(inp["x"])
+    rows, cols = sample_rows_cols(ref, wl.N, tile_n=512)
+    check_Y_sampled(bufs.Y, xb, inp["W"], ref, wl.k, rows, cols)
+
+
 def test_pair_and_single_modes_agree():
     wl = workloads.custom("modes", 1200, 256, 4, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=8)

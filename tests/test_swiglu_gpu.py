@@ -86,6 +86,26 @@ def test_swiglu_up_pair_mode(T, d, E, k, F):
     assert plan.info["tile_m"] == 256
 
 
+@pytest.mark.parametrize("T,d,E,k,F", [
+    (1000, 128, 2, 1, 272),   # 512-wide tiles: 256 gate + 256 up columns; 2 column tiles (256, 16)
+    (1200, 128, 3, 2, 640),   # 3 column tiles (256, 256, 128)
+])
+def test_swiglu_up_pair_mode_512_wide_tiles(T, d, E, k, F):
+    """Gated up-projection on 512-wide pair tiles: against the oracle, and H bit
+    for bit against 256-wide pair tiles (the same MMAs in the same K order)."""
+    plan = _up_check(T, d, E, k, F, 1, "none", tile_m=256, tile_n=512)
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 512
+    wl = workloads.custom("glu", T, d, E, k, 2 * F, 1, "none")
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    W1 = workloads.make_ffn_weights(wl, F, seed=0)[0].cuda()
+    H = {}
+    for tn in (256, 512):
+        _, bufs, rc, status = _run_up(wl, F, inp, W1, tile_m=256, tile_n=tn)
+        assert rc == 0, status
+        H[tn] = bufs.H.clone()
+    assert torch.equal(H[256].view(torch.int16), H[512].view(torch.int16))
+
+
 def test_swiglu_rejects_192_wide_tiles():
     wl = workloads.custom("g192", 100, 64, 4, 2, 384)
     plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, tile_n=192)
