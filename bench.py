@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -67,6 +68,20 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def kernel_code_hash(path: str = KERNEL_SRC) -> str:
+    """First 16 hex digits of the SHA-256 of the fused kernel's source with its
+    comments and blank lines removed: a comment edit keeps a capture valid, any
+    code change invalidates it."""
+    src = open(path, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = []
+    for line in src.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code.strip():
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def _traffic_per_launch(workload: str):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
     or None when absent or when the kernel source changed since the capture."""
@@ -78,8 +93,7 @@ def _traffic_per_launch(workload: str):
                 if ":" in line:
                     key, val = line.split(":", 1)
                     vals[key.strip()] = val.strip()
-        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
-        if vals.get("kernel_source_sha256_16") != src_hash:
+        if vals.get("kernel_code_sha256_16") != kernel_code_hash():
             return None
         return float(vals["traffic_bytes_per_launch"])
     except Exception:

@@ -1024,6 +1024,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // rows of A and 128 of the 256 columns of B in its own shared memory, and each
 // CTA's TMEM receives its 128 rows of the accumulator.  Per SM this halves the
 // B operand traffic (TMA writes into shared memory and MMA reads from it).
+// With BN = 512 (an opt-in tile width) a tile is 256 x 512: each K step issues
+// two N=256 MMAs into TMEM columns 0-255 and 256-511, each CTA holds 256 of the
+// 512 B columns, and the one 512-column accumulator fills TMEM (no overlap of a
+// tile's epilogue with the next tile's MMAs).
 //  * The leader claims tiles and writes each tile's description into both
 //    CTAs' schedule rings (the peer's through distributed shared memory).
 //  * Both CTAs' TMA loads complete on the leader's stage barrier; the

@@ -1,5 +1,6 @@
 """Host-side logic of bench.py without a GPU: the work model, the launch count,
-and the max-over-ranks aggregation across two gloo processes."""
+the kernel-code hash that ties the traffic summaries to the kernel, and the max-over-ranks
+aggregation across two gloo processes."""
 import os
 import socket
 
@@ -25,6 +26,17 @@ def test_algorithmic_work_mixtral():
 def test_launches_per_step():
     assert bench.launches_per_step(workloads.WORKLOADS["mixtral"]) == 3
     assert bench.launches_per_step(workloads.WORKLOADS["decode"]) == 2
+
+
+def test_kernel_code_hash_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("int f(int x) {\n    return x + 1;  // one\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("/* header */\n// f adds one\nint f(int x) {\n\n    return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) {\n    return x + 2;\n}\n")
+    assert bench.kernel_code_hash(str(a)) == bench.kernel_code_hash(str(b))
+    assert bench.kernel_code_hash(str(a)) != bench.kernel_code_hash(str(c))
 
 
 def _free_port():
