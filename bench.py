@@ -18,6 +18,7 @@ the timed region is bracketed by barriers and the max over ranks is used.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -101,29 +102,40 @@ def _traffic_per_launch(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler starts before the region (nvidia-smi takes a moment to report) and
+    keeps only the samples whose own timestamps fall between entry and exit."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    STARTUP_S = 0.5
+    PERIOD_MS = 50
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(self.STARTUP_S)
         except Exception:
             self.proc = None
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         self.lines = []
         if self.proc is not None:
+            time.sleep(2 * self.PERIOD_MS / 1000.0)  # the sample that covers the region's end
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -132,25 +144,38 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
+    @staticmethod
+    def _stamp(text: str):
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        rows = []
+        for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
+            t = self._stamp(parts[0])
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None
+                  and self.t0 <= r[0] <= self.t1 + self.PERIOD_MS / 1000.0]
+        window = "timed region"
+        if not inside and rows:  # no sample inside a very short region: the one nearest its end
+            stamped = [r for r in rows if r[0] is not None]
+            inside = [min(stamped, key=lambda r: abs(r[0] - self.t1))] if stamped else rows[-1:]
+            window = "nearest sample"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"}
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window,
+                "period_ms": self.PERIOD_MS}
 
 
 def algorithmic_work(wl, touched_experts: int):

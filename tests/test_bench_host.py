@@ -1,8 +1,10 @@
 """Host-side logic of bench.py without a GPU: the work model, the launch count,
 the kernel-code hash that ties the traffic summaries to the kernel, and the max-over-ranks
 aggregation across two gloo processes."""
+import datetime
 import os
 import socket
+import time
 
 import pytest
 import torch.distributed as dist
@@ -37,6 +39,34 @@ def test_kernel_code_hash_ignores_comments_only(tmp_path):
     c.write_text("int f(int x) {\n    return x + 2;\n}\n")
     assert bench.kernel_code_hash(str(a)) == bench.kernel_code_hash(str(b))
     assert bench.kernel_code_hash(str(a)) != bench.kernel_code_hash(str(c))
+
+
+def _smi_line(t, mhz, power_cap):
+    stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return f"{stamp}, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {power_cap}"
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region():
+    c = bench.ClockSampler(0)
+    c.t0 = time.time()
+    c.t1 = c.t0 + 0.3
+    c.lines = [_smi_line(c.t0 - 0.4, 1000, "Not Active"),   # before the region (idle)
+               _smi_line(c.t0 + 0.05, 2070, "Not Active"),
+               _smi_line(c.t0 + 0.15, 1900, "Active"),
+               _smi_line(c.t0 + 0.25, 1950, "Not Active"),
+               _smi_line(c.t0 + 0.9, 800, "Not Active")]    # after it
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1950.0 and s["window"] == "timed region"
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0
+
+
+def test_clock_summary_without_a_sample_inside_takes_the_nearest():
+    c = bench.ClockSampler(0)
+    c.t0 = time.time()
+    c.t1 = c.t0 + 0.01
+    c.lines = [_smi_line(c.t0 - 0.5, 1200, "Not Active"), _smi_line(c.t1 + 0.1, 2000, "Not Active")]
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 2000.0 and s["window"] == "nearest sample"
 
 
 def _free_port():
