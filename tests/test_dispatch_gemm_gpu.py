@@ -257,9 +257,10 @@ def _check_bf16(Y_bf16: np.ndarray, Yref: np.ndarray):
     assert (np.abs(Y_bf16 - Yref) <= 2.0 ** -8 * np.abs(Yref) + 1e-4 * rms).all()
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 256), (128, 128), (256, 0)])
-def test_bf16_output_full_parity_and_combine(tile_m, tile_n):
-    wl = workloads.custom("bf16", 1000, 256, 4, 2, 400, 2, "none")
+@pytest.mark.parametrize("tile_m,tile_n,N", [(128, 256, 400), (128, 128, 400), (256, 0, 400),
+                                            (256, 512, 1040)])  # 1040 = 2 x 512 + 16
+def test_bf16_output_full_parity_and_combine(tile_m, tile_n, N):
+    wl = workloads.custom("bf16", 1000, 256, 4, 2, N, 2, "none")
     inp = workloads.make_inputs(wl, seed=14)
     plan, bufs, rc, status = run_path(wl, inp, tile_m=tile_m, tile_n=tile_n, out_dtype=binding.MOE_OUT_BF16)
     assert rc == 0, status

@@ -13,11 +13,11 @@ from tests.gpu_util import check_route, check_Y
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
-def test_forward_replays_from_a_cuda_graph(tile_m):
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 0), (256, 0), (256, 512)])
+def test_forward_replays_from_a_cuda_graph(tile_m, tile_n):
     wl = workloads.custom("graph", 1200, 256, 8, 2, 512, 2, "zipf")
     inp = workloads.make_inputs(wl, seed=15)
-    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=tile_m)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=tile_m, tile_n=tile_n)
     bufs = binding.MoeBuffers(plan, "cuda")
     x, W, L = inp["x"].cuda(), inp["W"].cuda(), inp["logits"].cuda()
 

@@ -146,9 +146,10 @@ def test_grouped_gemm_full_parity(T, d, E, k, N, bias):
     _grouped_check(T, d, E, k, N, bias)
 
 
-def test_grouped_gemm_pair_mode():
-    plan = _grouped_check(1000, 128, 2, 1, 400, "none", tile_m=256)
-    assert plan.info["tile_m"] == 256
+@pytest.mark.parametrize("N,tile_n", [(400, 0), (1040, 512)])
+def test_grouped_gemm_pair_mode(N, tile_n):
+    plan = _grouped_check(1000, 128, 2, 1, N, "none", tile_m=256, tile_n=tile_n)
+    assert plan.info["tile_m"] == 256 and (tile_n == 0 or plan.info["tile_n"] == tile_n)
 
 
 def test_dispatch_and_grouped_calls_share_a_plan():

@@ -16,13 +16,14 @@ pytestmark = pytest.mark.gpu
 F = {name: i for i, name in enumerate(binding.TRACE_FIELDS)}
 
 
-@pytest.mark.parametrize("tile_m", [128, 256])
-def test_trace_records_are_consistent(tile_m):
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 0), (256, 0), (256, 512)])
+def test_trace_records_are_consistent(tile_m, tile_n):
     wl = workloads.custom("trace", 1200, 256, 8, 2, 512, 2, "zipf")
     inp = workloads.make_inputs(wl, seed=17)
-    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=tile_m)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=tile_m, tile_n=tile_n)
     bufs = binding.MoeBuffers(plan, "cuda")
     info = plan.info
+    assert tile_n == 0 or info["tile_n"] == tile_n
     trace = torch.full((info["sm_count"] * binding.TRACE_WORDS,), -1, dtype=torch.int64, device="cuda")
     binding.moe_set_trace(plan, trace)
     binding.forward(plan, inp["logits"].cuda(), inp["x"].cuda(), inp["W"].cuda(), bufs)
