@@ -617,8 +617,9 @@ def run_ours(args, wl):
         roof["peak_sustained"] = tf_sustained
         roof["frac_sustained"] = roof["achieved"] / tf_sustained
     roof["traffic"] = _traffic_per_launch(wl.name)
-    roof["kernel"] = ("dispatch_gemm_pair_kernel (CTA pairs, 256-row tiles)"
-                      if plan.info["tile_m"] == 256 else "dispatch_gemm_kernel (128-row tiles)")
+    tile = f"{plan.info['tile_m']}x{plan.info['tile_n']} tiles"
+    roof["kernel"] = (f"dispatch_gemm_pair_kernel (CTA pairs, {tile})"
+                      if plan.info["tile_m"] == 256 else f"dispatch_gemm_kernel ({tile})")
     roof["algorithmic_flops"] = flops
     roof["algorithmic_bytes"] = alg_bytes
     line = {
