@@ -57,6 +57,8 @@ struct TileInfo {
     int rows;  // valid rows 1..128; -1 marks the end of the schedule
     int rank;
     int arow;  // first row inside the rank's receive buffer
+    int m128;  // CTA pairs: 1 for an expert's last tile of at most 128 rows, run as an
+               // M=128 pair MMA (64 rows per CTA); 0 otherwise
 };
 
 constexpr int kMaxPieceBufs = 8;
@@ -555,6 +557,53 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
     }
 }
 
+// Epilogue of an M=128 pair tile for this CTA's 64 rows.  Such an MMA leaves, for
+// every 256-column MMA h of the tile, rows 0-63 of its columns [0, 128) in TMEM
+// lanes 0-63 and of its columns [128, 256) in lanes 64-127, all in TMEM columns
+// [256 h, 256 h + 128).  So lane quarter q holds rows 32 (q & 1) .. + 31 and
+// tile columns 256 h + 128 (q >> 1) + [0, 128).  `tacc`: the accumulator's TMEM
+// address.  Not used for gated tiles, whose gate and up columns would then lie
+// in different warps.
+__device__ __forceinline__ void epilogue_tile_m128(const DispatchGemmParams& p, const TileInfo& ti, int bn,
+                                                   uint32_t tacc, int q, int lane, float* epi) {
+    const int rb = q & 1, ch = q >> 1;
+    const int rows_valid = min(32, ti.rows - 32 * rb);
+    if (rows_valid <= 0) return;  // warp-uniform
+    const uint32_t tq = tacc + ((uint32_t)(32 * q) << 16);
+    const size_t row = (size_t)(ti.row0 + 32 * rb);
+    for (int h = 0; h < bn / 256; ++h) {
+        const int col0 = ti.n * bn + 256 * h + 128 * ch;  // first Y column of this warp's block
+        const int ncols = min(128, p.N - col0);
+        if (ncols <= 0) continue;
+        const uint32_t t0 = tq + (uint32_t)(256 * h);
+        if (p.out_bf16) {
+            uint16_t* ybase = static_cast<uint16_t*>(p.Y) + row * p.N + col0;
+            for (int c = 0; c < ncols; c += 64) {
+                uint32_t w[32];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[32];
+                    tmem_ld_32x32(t0 + (uint32_t)(c + 32 * hh), v);
+                    tmem_ld_wait(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[16 * hh + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                }
+                store_block_rows(epi, w, reinterpret_cast<float*>(ybase + c), (size_t)p.N / 2, rows_valid,
+                                 (ncols - c) / 2, lane);
+            }
+        } else {
+            float* ybase = static_cast<float*>(p.Y) + row * p.N + col0;
+            for (int c = 0; c < ncols; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32(t0 + (uint32_t)c, v);
+                tmem_ld_wait(v);
+                store_block_rows(epi, v, ybase + c, (size_t)p.N, rows_valid, ncols - c, lane);
+            }
+        }
+    }
+}
+
 // First column in W of the 64-column B box `j` of a tile whose columns start at
 // `ncol` (plain) or, in gated mode, whose gate and up halves each hold `half`
 // columns starting at F-column n * half: boxes [0, half/64) are gate columns,
@@ -614,7 +663,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
         const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
         if (tile >= total_tiles) {
-            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = 0;
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = 0;
             ti.rows = -1;
         } else {
             const int u = (int)(tile / (uint32_t)p.n_tiles);
@@ -638,6 +687,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             ti.rows = min(kTileM, cnt - ti.m * kTileM);
             ti.rank = e / e_per_rank;
             ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
+            ti.m128 = 0;
         }
         ctl->ring[slot] = ti;
         mbar_arrive(smem_addr(&ctl->sfull[slot]));
@@ -1046,6 +1096,7 @@ struct PairCfg {
     static constexpr int kBBytes = (BN / 2) * kTileK * 2;  // this CTA's BN/2 columns: 16 or 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 256);
+    static constexpr uint32_t kIdesc128 = idesc_bf16_f32_kmajA_mnmajB(kTileM, 256);  // tail tiles
     static constexpr int kTmemCols = 512;                // two 256-column accumulators or one of 512
     static constexpr int kAccs = 512 / BN;               // accumulators (TMEM double buffer for 256)
     static constexpr size_t kSmem =
@@ -1058,19 +1109,30 @@ struct PairCfg {
                   "scatter staging must stay inside the stage area");
 };
 
-// tile description of one CTA's half of a pair tile
+// Tile description of one CTA's half of a pair tile.  An expert's last pair tile
+// with at most 128 rows runs as an M=128 pair MMA (not in gated mode): each CTA
+// holds 64 of its rows (rows [64 half, 64 half + 64) of the 128-row tile 2 m2),
+// and both halves wait for that row tile's flag.
 __device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, int e, int m2,
                                int n, int half, TileInfo& ti) {
     const int e_per_rank = p.E / p.R;
     const int seg0 = __ldg(p.offsets + e);
     const int cnt = __ldg(p.offsets + e + 1) - seg0;
-    const int m = 2 * m2 + half;  // 128-row tile of this half
     ti.e = e;
-    ti.m = m;
     ti.n = n;
-    ti.row0 = seg0 + m * kTileM;
-    ti.rows = min(kTileM, cnt - m * kTileM);  // may be <= 0 for the odd half
-    ti.mtile = ti.rows > 0 ? mt_base[e] + m : -1;
+    ti.m128 = (!p.glu && cnt - 2 * kTileM * m2 <= kTileM) ? 1 : 0;
+    if (ti.m128) {
+        ti.m = 2 * m2;
+        ti.row0 = seg0 + ti.m * kTileM + (kTileM / 2) * half;
+        ti.rows = min(kTileM / 2, cnt - ti.m * kTileM - (kTileM / 2) * half);  // may be <= 0 for the odd half
+        ti.mtile = mt_base[e] + ti.m;
+    } else {
+        const int m = 2 * m2 + half;  // 128-row tile of this half
+        ti.m = m;
+        ti.row0 = seg0 + m * kTileM;
+        ti.rows = min(kTileM, cnt - m * kTileM);  // may be <= 0 for the odd half
+        ti.mtile = ti.rows > 0 ? mt_base[e] + m : -1;
+    }
     ti.rank = e / e_per_rank;
     ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
 }
@@ -1103,7 +1165,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
             TileInfo other;
             if (tile >= total_tiles) {
-                ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = 0;
+                ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = 0;
                 ti.e = -1;
                 other = ti;
             } else {
@@ -1229,6 +1291,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     while (ok) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 25, true, true)) break;
         const int e = ctl->ring[slot].e;
+        const uint32_t idesc = ctl->ring[slot].m128 ? C::kIdesc128 : C::kIdesc;
         mbar_arrive(smem_addr(&ctl->sempty[slot]));
         if (++slot == kRing) {
             slot = 0;
@@ -1252,7 +1315,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
                     const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
-                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
             }
             umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
@@ -1300,7 +1363,9 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 30, true, true);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
-        if (ti.rows - 32 * q > 0) {  // the odd half of a pair tile may hold fewer rows
+        if (ti.m128) {
+            epilogue_tile_m128(p, ti, C::kBN, tmem_base + (uint32_t)(acc * C::kBN), q, lane, epi);
+        } else if (ti.rows - 32 * q > 0) {  // the odd half of a pair tile may hold fewer rows
             const uint32_t tbase = tmem_base + (uint32_t)(acc * C::kBN) + ((uint32_t)(32 * q) << 16);
             epilogue_tile(p, ti, C::kBN, tbase, q, lane, epi);
         }

@@ -201,6 +201,16 @@ def test_pair_mode_512_wide_full_size(name):
     check_Y_sampled(bufs.Y, xb, inp["W"], ref, wl.k, rows, cols)
 
 
+@pytest.mark.parametrize("tile_n", [256, 512])
+@pytest.mark.parametrize("T", [257, 280, 320, 321, 356, 384, 385])
+def test_pair_mode_last_tile_of_at_most_128_rows(T, tile_n):
+    """One expert of T = 256 + r rows: its last pair tile holds r rows.  With r <= 128
+    it runs as an M=128 pair MMA, 64 rows per CTA (r = 1, 24, 64, 65, 100, 128); r =
+    129 is an ordinary pair tile with a short odd half.  Every row against the oracle."""
+    plan, _ = _full_check(workloads.custom("ptail", T, 128, 1, 1, 1024, 1, "none"), tile_m=256, tile_n=tile_n)
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == tile_n
+
+
 def test_pair_and_single_modes_agree():
     wl = workloads.custom("modes", 1200, 256, 4, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=8)
