@@ -288,6 +288,22 @@ def test_bf16_output_full_parity_and_combine(tile_m, tile_n, N):
     assert (np.abs(out.cpu().double().numpy() - want) <= bound + 1e-4 * rms).all()
 
 
+@pytest.mark.parametrize("tile_n", [256, 512])
+def test_bf16_output_on_m128_tail_tiles(tile_n):
+    """bf16 Y on pair tiles whose experts end in tails of at most 128 rows (about
+    300 rows per expert: one 256-row tile and an M=128 tail each)."""
+    wl = workloads.custom("bf16tail", 1200, 128, 8, 2, 1024, 2, "none")
+    inp = workloads.make_inputs(wl, seed=16)
+    plan, bufs, rc, status = run_path(wl, inp, tile_m=256, tile_n=tile_n, out_dtype=binding.MOE_OUT_BF16)
+    assert rc == 0, status
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    counts = np.diff(ref["offsets"])
+    assert ((counts % 256 > 0) & (counts % 256 <= 128)).sum() >= 4  # tail tiles present
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+    Yref = oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"])
+    _check_bf16(bufs.Y.float().cpu().double().numpy(), Yref)
+
+
 def test_bf16_output_mixtral_full_size_sampled():
     wl = workloads.WORKLOADS["mixtral"]
     inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
