@@ -1085,6 +1085,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //    accumulator-full barriers; both CTAs' epilogues release the accumulator
 //    on the leader's barrier.
 //  * Each CTA waits for the ready flag of its own 128-row half.
+//  * An expert's last tile of at most 128 rows runs as an M=128 pair MMA, 64
+//    rows per CTA, both CTAs waiting for that one row tile's flag
+//    (pair_half_info, epilogue_tile_m128).
 // The scatter role is unchanged; a pair takes one role ticket and its two
 // CTAs become scatter CTAs 2t and 2t+1.
 template <int STAGES, int BN>
