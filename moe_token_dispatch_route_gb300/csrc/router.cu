@@ -5,12 +5,24 @@
 // exact in fp32, so each step is one rounding), then the fp32 bias is added.
 //
 // CUDA cores, not tensor cores: the tensor cores' internal summation order is not
-// specified, and a different order can flip a near-tie in the top-k.  A block
-// computes TB tokens x EB experts; each thread owns one expert and P tokens (every
-// TB/P-th token, so the token groups of one warp read adjacent rows) with P
-// accumulators, P chosen so the grid fills the GPU; the next chunk is loaded into
-// registers while the current one is used; 32-wide chunks of x and W_r are staged in shared memory (x rows padded
-// to 36 floats, so the float4 reads of adjacent rows fall in different banks).
+// specified, and a different order can flip a near-tie in the top-k.
+//
+// Streamed kernel (E a multiple of 8, x and W_r 16-byte aligned): a thread owns one
+// token and Q consecutive experts (Q accumulators, each its own chain), a warp 32
+// tokens of one group of Q experts, a CTA of 4 warps NGB expert groups x 4/NGB
+// rows of 32 tokens.  The reduction runs in 64-element chunks through a 4-stage
+// cp.async ring in shared memory: the CTA's x rows (bf16, 136-byte rows, so the 32
+// lanes' 8-byte reads from 32 rows take two wavefronts) and W_r's chunk for the
+// CTA's experts (bf16, read as warp-wide broadcasts).  Per four reduction elements
+// a thread reads 8 bytes of x and four rows of its Q weights and runs 4Q FMAs.
+//
+// Fallback kernel (any E, 4-byte aligned x): a block computes TB tokens x EB
+// experts; each thread owns one expert and P tokens (every TB/P-th token, so the
+// token groups of one warp read adjacent rows) with P accumulators, P chosen so the
+// grid fills the GPU; the next chunk is loaded into registers while the current
+// one is used; 32-wide chunks of x and W_r are staged in shared memory (x rows
+// padded to 36 floats, so the float4 reads of adjacent rows fall in different
+// banks).
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -98,6 +110,113 @@ __global__ void __launch_bounds__(kRtThreads) router_logits_kernel(const RouterA
     }
 }
 
+constexpr int kRsThreads = 128;
+constexpr int kRsCh = 64;                 // reduction elements per stage (d is a multiple of 64)
+constexpr int kRsStages = 4;
+constexpr int kRsXStride = kRsCh + 4;     // bf16 per staged x row: 136 bytes
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+template <int Q, int NGB>  // experts per thread, expert groups per CTA
+constexpr size_t streamed_smem_bytes() {
+    return (size_t)kRsStages * (32 * (4 / NGB) * kRsXStride + kRsCh * Q * NGB) * 2;
+}
+
+template <int Q, int NGB>
+__global__ void __launch_bounds__(kRsThreads) router_logits_streamed(const RouterArgs a) {
+    constexpr int TB = 32 * (4 / NGB);             // tokens per CTA
+    constexpr int EBLK = Q * NGB;                  // experts per CTA
+    constexpr int XST = TB * kRsXStride;           // bf16 per x stage
+    constexpr int WST = kRsCh * EBLK;              // bf16 per W stage
+    constexpr int XCOPIES = TB * kRsCh / 4;        // 8-byte copies of x per stage
+    constexpr int WCOPIES = kRsCh * EBLK / 8;      // 16-byte copies of W per stage
+    static_assert(EBLK % 8 == 0, "W rows are copied 8 experts (16 bytes) at a time");
+    extern __shared__ __align__(16) uint16_t rs[];
+    uint16_t* Xs = rs;                             // [kRsStages][TB][kRsXStride]
+    uint16_t* Ws = rs + kRsStages * XST;           // [kRsStages][kRsCh][EBLK]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = warp % NGB;                    // this warp's expert group
+    const int tl = (warp / NGB) * 32 + lane;       // this thread's token inside the CTA
+    const int t0 = blockIdx.x * TB, e0 = blockIdx.y * EBLK;
+    const int nch = a.d / kRsCh;
+
+    auto load_stage = [&](int st, int c) {
+        const uint32_t xs = smem_addr(Xs + st * XST), ws = smem_addr(Ws + st * WST);
+        for (int j = tid; j < XCOPIES; j += kRsThreads) {
+            const int r = j / (kRsCh / 4), part = j % (kRsCh / 4);
+            const int t = t0 + r;
+            const uint16_t* src = a.x + (t < a.T ? (size_t)t * a.d + (size_t)c * kRsCh + part * 4 : 0);
+            cp_async8(xs + (uint32_t)(r * kRsXStride + part * 4) * 2, src, t < a.T ? 8 : 0);
+        }
+        for (int j = tid; j < WCOPIES; j += kRsThreads) {
+            const int i = j / (EBLK / 8), part = j % (EBLK / 8);
+            const int e = e0 + part * 8;
+            const uint16_t* src = a.Wr + (e < a.E ? (size_t)(c * kRsCh + i) * a.E + e : 0);
+            cp_async16_cg_zfill(ws + (uint32_t)(i * EBLK + part * 8) * 2, src, e < a.E ? 16 : 0);
+        }
+    };
+
+    float acc[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) acc[q] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kRsStages - 1; ++c) {
+        if (c < nch) load_stage(c, c);
+        cp_async_commit();
+    }
+    for (int c = 0; c < nch; ++c) {
+        cp_async_wait<kRsStages - 2>();
+        __syncthreads();  // chunk c is in; every thread is done with chunk c - 1's stage
+        const int cn = c + kRsStages - 1;
+        if (cn < nch) load_stage(cn % kRsStages, cn);
+        cp_async_commit();
+        const uint16_t* xr = Xs + (c % kRsStages) * XST + tl * kRsXStride;
+        const uint16_t* wr = Ws + (c % kRsStages) * WST + grp * Q;
+#pragma unroll 4
+        for (int ii = 0; ii < kRsCh; ii += 4) {
+            const uint2 xv = *reinterpret_cast<const uint2*>(xr + ii);
+            const float xf[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
+                                 __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t wv[Q / 2];
+                if constexpr (Q == 8) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(wr + (ii + k) * EBLK);
+                    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+                } else {
+                    const uint2 w2 = *reinterpret_cast<const uint2*>(wr + (ii + k) * EBLK);
+                    wv[0] = w2.x; wv[1] = w2.y;
+                }
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {  // element i = chunk + ii + k: i ascending per accumulator
+                    const uint32_t h = wv[q / 2];
+                    const float w = __uint_as_float((q & 1) ? (h & 0xFFFF0000u) : (h << 16));
+                    acc[q] = fmaf(xf[k], w, acc[q]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    const int t = t0 + tl;
+    if (t < a.T) {
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int e = e0 + grp * Q + q;
+            if (e < a.E) a.L[(size_t)t * a.E + e] = a.bias ? acc[q] + __ldg(a.bias + e) : acc[q];
+        }
+    }
+}
+
+template <int Q, int NGB>
+cudaError_t launch_streamed(const RouterArgs& a, cudaStream_t stream) {
+    constexpr int TB = 32 * (4 / NGB), EBLK = Q * NGB;
+    const dim3 grid((a.T + TB - 1) / TB, (a.E + EBLK - 1) / EBLK);
+    router_logits_streamed<Q, NGB><<<grid, kRsThreads, streamed_smem_bytes<Q, NGB>(), stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int EB, int P>
 cudaError_t launch_rt(const RouterArgs& a, cudaStream_t stream) {
     constexpr int TB = (kRtThreads / 32) * (32 / EB) * P;
@@ -123,6 +242,16 @@ cudaError_t launch_rt_p(const RouterArgs& a, cudaStream_t stream) {
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
     if (a.d % kRtChunk != 0) return cudaErrorInvalidValue;
+    const bool streamed = a.E % 8 == 0 && a.d % kRsCh == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
+                          (reinterpret_cast<uintptr_t>(a.Wr) & 15) == 0;
+    if (streamed) {
+        // 8 experts per thread for wide routers on large batches, else 4 (more CTAs);
+        // expert groups per CTA: 4 when there are that many, else 2
+        const int q = (a.E >= 64 && a.T >= 512) ? 8 : 4;
+        const int ngb = a.E / q >= 4 ? 4 : 2;
+        if (q == 8) return ngb == 4 ? launch_streamed<8, 4>(a, stream) : launch_streamed<8, 2>(a, stream);
+        return ngb == 4 ? launch_streamed<4, 4>(a, stream) : launch_streamed<4, 2>(a, stream);
+    }
     if (a.E <= 8) return launch_rt_p<8>(a, stream);
     if (a.E <= 16) return launch_rt_p<16>(a, stream);
     return launch_rt_p<32>(a, stream);

@@ -37,11 +37,31 @@ def _bits(a):
 @pytest.mark.parametrize("T,d,E,bias", [
     (1, 64, 1, "none"), (100, 128, 3, "none"), (257, 256, 8, "none"), (300, 192, 17, "zipf"),
     (64, 512, 128, "hot4"), (70, 64, 1024, "none"), (1000, 2048, 64, "zipf"),
+    (333, 128, 24, "none"),    # streamed kernel: 16-expert blocks, the last one half outside E
+    (700, 64, 40, "zipf"),     # streamed: 40 experts in blocks of 16
+    (520, 256, 256, "none"),   # streamed: 8 experts per thread
+    (31, 4096, 16, "none"),    # streamed: a single partial row of tokens, a long reduction
 ])
 def test_router_logits_bit_exact(T, d, E, bias):
     wl = workloads.custom("router", T, d, E, 1, 16, 1, bias)
     inp = workloads.make_inputs(wl, seed=14, with_weights=False)
     _, L = _gpu_logits(wl, inp)
+    assert np.array_equal(_bits(L.cpu().numpy()), _bits(_oracle_logits(wl, inp)))
+
+
+@pytest.mark.parametrize("E", [8, 64])
+def test_router_logits_unaligned_inputs_take_the_fallback_kernel(E):
+    """x at a 4-byte (not 16-byte) offset: the scalar fallback kernel, bit-exact too."""
+    wl = workloads.custom("router_unaligned", 200, 256, E, 1, 16, 1, "none")
+    inp = workloads.make_inputs(wl, seed=15, with_weights=False)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N)
+    raw = torch.empty(wl.T * wl.d + 2, dtype=torch.bfloat16, device="cuda")
+    x = raw[2:].view(wl.T, wl.d)
+    x.copy_(inp["x"])
+    assert x.data_ptr() % 16 == 4
+    L = torch.full((wl.T, wl.E), float("nan"), dtype=torch.float32, device="cuda")
+    binding.moe_router_logits(plan, x, inp["W_r"].cuda(), None, L)
+    torch.cuda.synchronize()
     assert np.array_equal(_bits(L.cpu().numpy()), _bits(_oracle_logits(wl, inp)))
 
 
