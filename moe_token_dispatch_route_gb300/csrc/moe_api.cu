@@ -249,7 +249,7 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->ws.total = off;
 
     if ((!p->pair && dispatch_gemm_prepare_attributes(p->tile_n, p->stages, p->smem) != cudaSuccess) ||
-        route_prepare_attributes() != cudaSuccess) {
+        route_prepare_attributes() != cudaSuccess || router_prepare_attributes() != cudaSuccess) {
         cudaGetLastError();
         delete p;
         return MOE_ERR_CUDA;

@@ -129,6 +129,7 @@ struct RouterArgs {
     int sm_count;
 };
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream);
+cudaError_t router_prepare_attributes();  // shared-memory opt-in of the router kernels
 
 struct CombineArgs {
     const void* Y;        // [S][N] destination order, fp32 or bf16

@@ -7,14 +7,21 @@
 // CUDA cores, not tensor cores: the tensor cores' internal summation order is not
 // specified, and a different order can flip a near-tie in the top-k.
 //
-// Streamed kernel (E a multiple of 8, x and W_r 16-byte aligned): a thread owns one
-// token and Q consecutive experts (Q accumulators, each its own chain), a warp 32
-// tokens of one group of Q experts, a CTA of 4 warps NGB expert groups x 4/NGB
-// rows of 32 tokens.  The reduction runs in 64-element chunks through a 4-stage
-// cp.async ring in shared memory: the CTA's x rows (bf16, 136-byte rows, so the 32
-// lanes' 8-byte reads from 32 rows take two wavefronts) and W_r's chunk for the
-// CTA's experts (bf16, read as warp-wide broadcasts).  Per four reduction elements
-// a thread reads 8 bytes of x and four rows of its Q weights and runs 4Q FMAs.
+// Streamed kernel (E a multiple of 8, d of 64, x and W_r 16-byte aligned): a
+// thread owns P tokens and Q consecutive experts (P x Q accumulators, each its own
+// chain), a warp 32 token rows of one group of Q experts, a CTA NGB expert groups x
+// WPG warp rows.  The reduction runs in CH-element chunks through a 4-stage
+// cp.async ring in shared memory holding the CTA's x rows (bf16, rows padded by 8
+// bytes, so the 32 lanes' 8-byte reads from 32 rows take two wavefronts) and W_r's
+// chunk for the CTA's experts; each chunk of W_r is widened to fp32 once per CTA
+// and then read as warp-wide broadcasts.  The chunk loop is unrolled whole, so
+// shared-memory loads run ahead of the FMA chains.  Two shapes:
+//   wide   (P 2, Q 8, 128 tokens x 32 experts per CTA of 8 warps, CH 64), once its
+//          grid covers every SM: one fp32 weight read feeds 16 FMAs, so shared-memory
+//          wavefronts stay below the FMA issue rate;
+//   narrow (P 1, Q 2, 32 tokens x 8 experts per CTA of 4 warps, CH 128): small
+//          batches and few experts, where the work is a few warps per SM and the
+//          time goes to the chains' latency and the per-chunk barriers.
 //
 // Fallback kernel (any E, 4-byte aligned x): a block computes TB tokens x EB
 // experts; each thread owns one expert and P tokens (every TB/P-th token, so the
@@ -110,57 +117,81 @@ __global__ void __launch_bounds__(kRtThreads) router_logits_kernel(const RouterA
     }
 }
 
-constexpr int kRsThreads = 128;
-constexpr int kRsCh = 64;                 // reduction elements per stage (d is a multiple of 64)
 constexpr int kRsStages = 4;
-constexpr int kRsXStride = kRsCh + 4;     // bf16 per staged x row: 136 bytes
 
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-template <int Q, int NGB>  // experts per thread, expert groups per CTA
-constexpr size_t streamed_smem_bytes() {
-    return (size_t)kRsStages * (32 * (4 / NGB) * kRsXStride + kRsCh * Q * NGB) * 2;
-}
-
-template <int Q, int NGB>
-__global__ void __launch_bounds__(kRsThreads) router_logits_streamed(const RouterArgs a) {
-    constexpr int TB = 32 * (4 / NGB);             // tokens per CTA
-    constexpr int EBLK = Q * NGB;                  // experts per CTA
-    constexpr int XST = TB * kRsXStride;           // bf16 per x stage
-    constexpr int WST = kRsCh * EBLK;              // bf16 per W stage
-    constexpr int XCOPIES = TB * kRsCh / 4;        // 8-byte copies of x per stage
-    constexpr int WCOPIES = kRsCh * EBLK / 8;      // 16-byte copies of W per stage
+// Streamed-kernel shape: Q experts x P tokens per thread, NGB expert groups and
+// WPG warp rows per CTA, CH reduction elements per ring stage.
+template <int Q_, int P_, int NGB_, int WPG_, int CH_>
+struct RsCfg {
+    static constexpr int Q = Q_, P = P_, NGB = NGB_, WPG = WPG_, CH = CH_;
+    static constexpr int kThreads = 32 * NGB * WPG;
+    static constexpr int TB = 32 * WPG * P;      // tokens per CTA
+    static constexpr int EBLK = Q * NGB;         // experts per CTA
+    static constexpr int XS = CH + 4;            // bf16 per staged x row (2 * CH + 8 bytes)
+    static constexpr int XST = TB * XS;          // bf16 per x stage
+    static constexpr int WST = CH * EBLK;        // bf16 per W stage
+    static constexpr size_t kSmem = (size_t)kRsStages * (XST + WST) * 2 + (size_t)WST * 4;
     static_assert(EBLK % 8 == 0, "W rows are copied 8 experts (16 bytes) at a time");
+    static_assert(Q == 2 || Q % 4 == 0, "a thread's Q weights are read as float2 or float4 words");
+    static_assert(CH % 4 == 0, "x is read four elements at a time");
+};
+
+// Q consecutive fp32 weights of one reduction element
+template <int Q>
+__device__ __forceinline__ void weights_f32(const float* p, float (&w)[Q]) {
+    if constexpr (Q == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+#pragma unroll
+        for (int u = 0; u < Q / 4; ++u) {
+            const float4 v = *reinterpret_cast<const float4*>(p + 4 * u);
+            w[4 * u] = v.x; w[4 * u + 1] = v.y; w[4 * u + 2] = v.z; w[4 * u + 3] = v.w;
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads) router_logits_streamed(const RouterArgs a) {
+    constexpr int Q = C::Q, P = C::P, NGB = C::NGB, WPG = C::WPG, CH = C::CH;
+    constexpr int NT = C::kThreads, TB = C::TB, EBLK = C::EBLK, XS = C::XS, XST = C::XST, WST = C::WST;
+    constexpr int XCOPIES = TB * CH / 4;           // 8-byte copies of x per stage
+    constexpr int WCOPIES = WST / 8;               // 16-byte copies of W per stage
     extern __shared__ __align__(16) uint16_t rs[];
-    uint16_t* Xs = rs;                             // [kRsStages][TB][kRsXStride]
-    uint16_t* Ws = rs + kRsStages * XST;           // [kRsStages][kRsCh][EBLK]
+    uint16_t* Xs = rs;                             // [kRsStages][TB][XS]
+    uint16_t* Ws = rs + kRsStages * XST;           // [kRsStages][CH][EBLK]
+    float* Wf = reinterpret_cast<float*>(Ws + kRsStages * WST);  // [CH][EBLK], the current chunk
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = warp % NGB;                    // this warp's expert group
-    const int tl = (warp / NGB) * 32 + lane;       // this thread's token inside the CTA
+    const int tl = (warp / NGB) * 32 + lane;       // this thread's first token inside the CTA
     const int t0 = blockIdx.x * TB, e0 = blockIdx.y * EBLK;
-    const int nch = a.d / kRsCh;
+    const int nch = a.d / CH;
 
     auto load_stage = [&](int st, int c) {
         const uint32_t xs = smem_addr(Xs + st * XST), ws = smem_addr(Ws + st * WST);
-        for (int j = tid; j < XCOPIES; j += kRsThreads) {
-            const int r = j / (kRsCh / 4), part = j % (kRsCh / 4);
+        for (int j = tid; j < XCOPIES; j += NT) {
+            const int r = j / (CH / 4), part = j % (CH / 4);
             const int t = t0 + r;
-            const uint16_t* src = a.x + (t < a.T ? (size_t)t * a.d + (size_t)c * kRsCh + part * 4 : 0);
-            cp_async8(xs + (uint32_t)(r * kRsXStride + part * 4) * 2, src, t < a.T ? 8 : 0);
+            const uint16_t* src = a.x + (t < a.T ? (size_t)t * a.d + (size_t)c * CH + part * 4 : 0);
+            cp_async8(xs + (uint32_t)(r * XS + part * 4) * 2, src, t < a.T ? 8 : 0);
         }
-        for (int j = tid; j < WCOPIES; j += kRsThreads) {
+        for (int j = tid; j < WCOPIES; j += NT) {
             const int i = j / (EBLK / 8), part = j % (EBLK / 8);
             const int e = e0 + part * 8;
-            const uint16_t* src = a.Wr + (e < a.E ? (size_t)(c * kRsCh + i) * a.E + e : 0);
+            const uint16_t* src = a.Wr + (e < a.E ? (size_t)(c * CH + i) * a.E + e : 0);
             cp_async16_cg_zfill(ws + (uint32_t)(i * EBLK + part * 8) * 2, src, e < a.E ? 16 : 0);
         }
     };
 
-    float acc[Q];
+    float acc[P][Q];
 #pragma unroll
-    for (int q = 0; q < Q; ++q) acc[q] = 0.f;
+    for (int p = 0; p < P; ++p)
+#pragma unroll
+        for (int q = 0; q < Q; ++q) acc[p][q] = 0.f;
 #pragma unroll
     for (int c = 0; c < kRsStages - 1; ++c) {
         if (c < nch) load_stage(c, c);
@@ -168,54 +199,81 @@ __global__ void __launch_bounds__(kRsThreads) router_logits_streamed(const Route
     }
     for (int c = 0; c < nch; ++c) {
         cp_async_wait<kRsStages - 2>();
-        __syncthreads();  // chunk c is in; every thread is done with chunk c - 1's stage
+        __syncthreads();  // chunk c is in; every thread is done with chunk c - 1 (and Wf)
         const int cn = c + kRsStages - 1;
         if (cn < nch) load_stage(cn % kRsStages, cn);
         cp_async_commit();
-        const uint16_t* xr = Xs + (c % kRsStages) * XST + tl * kRsXStride;
-        const uint16_t* wr = Ws + (c % kRsStages) * WST + grp * Q;
-#pragma unroll 4
-        for (int ii = 0; ii < kRsCh; ii += 4) {
-            const uint2 xv = *reinterpret_cast<const uint2*>(xr + ii);
-            const float xf[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                                 __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
+        {  // widen the chunk's weights once; each is used by the CTA's TB tokens
+            const uint4* src = reinterpret_cast<const uint4*>(Ws + (c % kRsStages) * WST);
+            float4* dst = reinterpret_cast<float4*>(Wf);
+            for (int j = tid; j < WST / 8; j += NT) {
+                const uint4 v = src[j];
+                dst[2 * j] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                         __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+                dst[2 * j + 1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                             __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+            }
+        }
+        __syncthreads();
+        const uint16_t* xr = Xs + (c % kRsStages) * XST + tl * XS;
+        const float* wr = Wf + grp * Q;
+#pragma unroll
+        for (int ii = 0; ii < CH; ii += 4) {  // unrolled whole, so the loads run ahead of the FMAs
+            float xf[P][4];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {  // token p of this thread: row tl + 32 * WPG * p
+                const uint2 xv = *reinterpret_cast<const uint2*>(xr + p * 32 * WPG * XS + ii);
+                xf[p][0] = __uint_as_float(xv.x << 16);
+                xf[p][1] = __uint_as_float(xv.x & 0xFFFF0000u);
+                xf[p][2] = __uint_as_float(xv.y << 16);
+                xf[p][3] = __uint_as_float(xv.y & 0xFFFF0000u);
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                uint32_t wv[Q / 2];
-                if constexpr (Q == 8) {
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(wr + (ii + k) * EBLK);
-                    wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-                } else {
-                    const uint2 w2 = *reinterpret_cast<const uint2*>(wr + (ii + k) * EBLK);
-                    wv[0] = w2.x; wv[1] = w2.y;
-                }
+                float w[Q];
+                weights_f32<Q>(wr + (ii + k) * EBLK, w);
 #pragma unroll
-                for (int q = 0; q < Q; ++q) {  // element i = chunk + ii + k: i ascending per accumulator
-                    const uint32_t h = wv[q / 2];
-                    const float w = __uint_as_float((q & 1) ? (h & 0xFFFF0000u) : (h << 16));
-                    acc[q] = fmaf(xf[k], w, acc[q]);
-                }
+                for (int p = 0; p < P; ++p)
+#pragma unroll
+                    for (int q = 0; q < Q; ++q)  // element i = chunk + ii + k: i ascending per accumulator
+                        acc[p][q] = fmaf(xf[p][k], w[q], acc[p][q]);
             }
         }
     }
     cp_async_wait<0>();
-    const int t = t0 + tl;
-    if (t < a.T) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const int t = t0 + tl + 32 * WPG * p;
+        if (t >= a.T) continue;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             const int e = e0 + grp * Q + q;
-            if (e < a.E) a.L[(size_t)t * a.E + e] = a.bias ? acc[q] + __ldg(a.bias + e) : acc[q];
+            if (e < a.E) a.L[(size_t)t * a.E + e] = a.bias ? acc[p][q] + __ldg(a.bias + e) : acc[p][q];
         }
     }
 }
 
-template <int Q, int NGB>
+template <class C>
+cudaError_t streamed_attributes() {
+    if (C::kSmem <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(router_logits_streamed<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)C::kSmem);
+}
+
+template <class C>
 cudaError_t launch_streamed(const RouterArgs& a, cudaStream_t stream) {
-    constexpr int TB = 32 * (4 / NGB), EBLK = Q * NGB;
-    const dim3 grid((a.T + TB - 1) / TB, (a.E + EBLK - 1) / EBLK);
-    router_logits_streamed<Q, NGB><<<grid, kRsThreads, streamed_smem_bytes<Q, NGB>(), stream>>>(a);
+    const dim3 grid((a.T + C::TB - 1) / C::TB, (a.E + C::EBLK - 1) / C::EBLK);
+    router_logits_streamed<C><<<grid, C::kThreads, C::kSmem, stream>>>(a);
     return cudaGetLastError();
 }
+
+// The streamed shapes.  Wide: 8 experts x 2 tokens per thread, 128 tokens x 32
+// experts per CTA of 8 warps (each weight read from shared memory feeds 16 FMAs).
+// Narrow: 2 experts x 1 token per thread, 32 tokens x 8 experts per CTA of 4 warps,
+// 128-element stages (more and shorter chains, for small batches and few experts).
+using RsWide = RsCfg<8, 2, 4, 2, 64>;
+using RsNarrow = RsCfg<2, 1, 4, 1, 128>;
+using RsNarrow64 = RsCfg<2, 1, 4, 1, 64>;  // d not a multiple of 128
 
 template <int EB, int P>
 cudaError_t launch_rt(const RouterArgs& a, cudaStream_t stream) {
@@ -239,18 +297,25 @@ cudaError_t launch_rt_p(const RouterArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t router_prepare_attributes() {
+    cudaError_t e = streamed_attributes<RsWide>();
+    if (e == cudaSuccess) e = streamed_attributes<RsNarrow>();
+    if (e == cudaSuccess) e = streamed_attributes<RsNarrow64>();
+    return e;
+}
+
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
     if (a.d % kRtChunk != 0) return cudaErrorInvalidValue;
-    const bool streamed = a.E % 8 == 0 && a.d % kRsCh == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
+    const bool streamed = a.E % 8 == 0 && a.d % 64 == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
                           (reinterpret_cast<uintptr_t>(a.Wr) & 15) == 0;
     if (streamed) {
-        // 8 experts per thread for wide routers on large batches, else 4 (more CTAs);
-        // expert groups per CTA: 4 when there are that many, else 2
-        const int q = (a.E >= 64 && a.T >= 512) ? 8 : 4;
-        const int ngb = a.E / q >= 4 ? 4 : 2;
-        if (q == 8) return ngb == 4 ? launch_streamed<8, 4>(a, stream) : launch_streamed<8, 2>(a, stream);
-        return ngb == 4 ? launch_streamed<4, 4>(a, stream) : launch_streamed<4, 2>(a, stream);
+        // the wide shape once its grid covers every SM, else the narrow one
+        const long long wide_ctas = (long long)((a.T + RsWide::TB - 1) / RsWide::TB) *
+                                    ((a.E + RsWide::EBLK - 1) / RsWide::EBLK);
+        if (a.E >= RsWide::EBLK && wide_ctas >= a.sm_count) return launch_streamed<RsWide>(a, stream);
+        if (a.d % RsNarrow::CH == 0) return launch_streamed<RsNarrow>(a, stream);
+        return launch_streamed<RsNarrow64>(a, stream);
     }
     if (a.E <= 8) return launch_rt_p<8>(a, stream);
     if (a.E <= 16) return launch_rt_p<16>(a, stream);

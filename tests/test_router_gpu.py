@@ -37,10 +37,14 @@ def _bits(a):
 @pytest.mark.parametrize("T,d,E,bias", [
     (1, 64, 1, "none"), (100, 128, 3, "none"), (257, 256, 8, "none"), (300, 192, 17, "zipf"),
     (64, 512, 128, "hot4"), (70, 64, 1024, "none"), (1000, 2048, 64, "zipf"),
-    (333, 128, 24, "none"),    # streamed kernel: 16-expert blocks, the last one half outside E
-    (700, 64, 40, "zipf"),     # streamed: 40 experts in blocks of 16
-    (520, 256, 256, "none"),   # streamed: 8 experts per thread
+    (333, 128, 24, "none"),    # streamed, narrow shape: 8-expert blocks, 128-element stages
+    (700, 64, 40, "zipf"),     # streamed, narrow shape with 64-element stages (d = 64)
+    (520, 256, 256, "none"),   # streamed, narrow shape: too few CTAs for the wide one
     (31, 4096, 16, "none"),    # streamed: a single partial row of tokens, a long reduction
+    # streamed, wide shape (128 tokens x 32 experts per CTA, grid of at least 152 CTAs):
+    (10000, 128, 40, "zipf"),  # the second expert block holds 8 experts, the last token block 16 tokens
+    (19457, 64, 32, "none"),   # the last CTA holds 1 token (its second-token rows all past T); one stage
+    (4864, 192, 256, "hot4"),  # three stages, fewer than the ring's depth
 ])
 def test_router_logits_bit_exact(T, d, E, bias):
     wl = workloads.custom("router", T, d, E, 1, 16, 1, bias)
