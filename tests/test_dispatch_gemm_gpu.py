@@ -211,6 +211,25 @@ def test_pair_mode_last_tile_of_at_most_128_rows(T, tile_n):
     assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == tile_n
 
 
+@pytest.mark.parametrize("T,E,k,N", [
+    (1000, 4, 2, 384),    # 384 = 256 + 128: the last column tile exactly 128 wide
+    (1000, 4, 2, 640),    # 640 = 512 + 128
+    (1200, 8, 2, 528),    # a 16-wide last tile; ~300-row experts, so M=128 tails (not narrow) too
+    (1500, 4, 2, 1408),   # six column tiles, the last 128 wide
+])
+def test_pair_mode_narrow_last_column_tile(T, E, k, N):
+    """256-wide pair tiles whose last column tile holds at most 128 columns run it as an
+    N=128 pair MMA, one 64-column B box per CTA.  Against the oracle, and (where 512-wide
+    tiles exist, N >= 512) bit for bit against 512-wide tiles, which issue N=256 MMAs
+    only: each element sees the same K order."""
+    wl = workloads.custom("narrow", T, 128, E, k, N, 1, "none")
+    plan, bufs = _full_check(wl, tile_m=256, tile_n=256)
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
+    if N >= 512:
+        _, bufs512 = _full_check(wl, tile_m=256, tile_n=512)
+        assert torch.equal(bufs.Y, bufs512.Y)
+
+
 def test_pair_and_single_modes_agree():
     wl = workloads.custom("modes", 1200, 256, 4, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=8)
@@ -268,7 +287,8 @@ def _check_bf16(Y_bf16: np.ndarray, Yref: np.ndarray):
 
 
 @pytest.mark.parametrize("tile_m,tile_n,N", [(128, 256, 400), (128, 128, 400), (256, 0, 400),
-                                            (256, 512, 1040)])  # 1040 = 2 x 512 + 16
+                                            (256, 512, 1040),   # 1040 = 2 x 512 + 16
+                                            (256, 256, 384)])   # a narrow (N=128) last column tile
 def test_bf16_output_full_parity_and_combine(tile_m, tile_n, N):
     wl = workloads.custom("bf16", 1000, 256, 4, 2, N, 2, "none")
     inp = workloads.make_inputs(wl, seed=14)
