@@ -59,8 +59,6 @@ struct TileInfo {
     int arow;  // first row inside the rank's receive buffer
     int m128;  // CTA pairs: 1 for an expert's last tile of at most 128 rows, run as an
                // M=128 pair MMA (64 rows per CTA); 0 otherwise
-    int narrow;  // CTA pairs, 256-wide tiles: 1 for a last column tile of at most 128
-                 // columns, run as an N=128 pair MMA; 0 otherwise
 };
 
 constexpr int kMaxPieceBufs = 8;
@@ -665,7 +663,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
         const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
         if (tile >= total_tiles) {
-            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = ti.narrow = 0;
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = 0;
             ti.rows = -1;
         } else {
             const int u = (int)(tile / (uint32_t)p.n_tiles);
@@ -690,7 +688,6 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             ti.rank = e / e_per_rank;
             ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
             ti.m128 = 0;
-            ti.narrow = 0;
         }
         ctl->ring[slot] = ti;
         mbar_arrive(smem_addr(&ctl->sfull[slot]));
@@ -1091,10 +1088,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * An expert's last tile of at most 128 rows runs as an M=128 pair MMA, 64
 //    rows per CTA, both CTAs waiting for that one row tile's flag
 //    (pair_half_info, epilogue_tile_m128).
-//  * With 256-wide tiles, a last column tile of at most 128 columns (N not a
-//    multiple of 256) runs as an N=128 pair MMA: each CTA loads one 64-column
-//    B box instead of two, and the MMA does half the work.  Not for M=128 or
-//    gated tiles.
 // The scatter role is unchanged; a pair takes one role ticket and its two
 // CTAs become scatter CTAs 2t and 2t+1.
 template <int STAGES, int BN>
@@ -1107,7 +1100,6 @@ struct PairCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 256);
     static constexpr uint32_t kIdesc128 = idesc_bf16_f32_kmajA_mnmajB(kTileM, 256);  // tail tiles
-    static constexpr uint32_t kIdescN128 = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 128);  // narrow tiles
     static constexpr int kTmemCols = 512;                // two 256-column accumulators or one of 512
     static constexpr int kAccs = 512 / BN;               // accumulators (TMEM double buffer for 256)
     static constexpr size_t kSmem =
@@ -1177,7 +1169,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             TileInfo other;
             if (tile >= total_tiles) {
                 ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = 0;
-                ti.narrow = 0;
                 ti.e = -1;
                 other = ti;
             } else {
@@ -1189,8 +1180,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 const int m2 = local % pt_e;
                 pair_half_info(p, mt_base, e, m2, n, 0, ti);
                 pair_half_info(p, mt_base, e, m2, n, 1, other);
-                ti.narrow = other.narrow =
-                    (BN == 256 && !p.glu && !ti.m128 && p.N - n * BN <= BN / 2) ? 1 : 0;
             }
             ctl->ring[slot] = ti;
             const int* o = reinterpret_cast<const int*>(&other);
@@ -1245,10 +1234,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
             for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, cur.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
-        // a narrow tile (N=128 MMA): each CTA holds 64 of its 128 columns, box 0 or 1
-        const int nbox = cur.narrow ? 1 : 2 * C::kHalves;
-        if (cur.narrow) bcol[0] = b_box_col(p, cur.n, C::kBN, leader ? 0 : 1);
-        const uint32_t stage_tx = 2u * (uint32_t)(C::kABytes + 8192 * nbox);  // both CTAs' bytes
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -1267,13 +1252,12 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             }
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
-            if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
             tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
 #pragma unroll
             for (int b = 0; b < 2 * C::kHalves; ++b)
-                if (b < nbox)
-                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
-                                     brow + kb * kTileK);
+                tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                 brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -1310,8 +1294,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     while (ok) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 25, true, true)) break;
         const int e = ctl->ring[slot].e;
-        const uint32_t idesc =
-            ctl->ring[slot].m128 ? C::kIdesc128 : ctl->ring[slot].narrow ? C::kIdescN128 : C::kIdesc;
+        const uint32_t idesc = ctl->ring[slot].m128 ? C::kIdesc128 : C::kIdesc;
         mbar_arrive(smem_addr(&ctl->sempty[slot]));
         if (++slot == kRing) {
             slot = 0;

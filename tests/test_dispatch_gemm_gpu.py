@@ -218,10 +218,9 @@ def test_pair_mode_last_tile_of_at_most_128_rows(T, tile_n):
     (1500, 4, 2, 1408),   # six column tiles, the last 128 wide
 ])
 def test_pair_mode_narrow_last_column_tile(T, E, k, N):
-    """256-wide pair tiles whose last column tile holds at most 128 columns run it as an
-    N=128 pair MMA, one 64-column B box per CTA.  Against the oracle, and (where 512-wide
-    tiles exist, N >= 512) bit for bit against 512-wide tiles, which issue N=256 MMAs
-    only: each element sees the same K order."""
+    """256-wide pair tiles whose last column tile holds at most 128 columns (its B boxes
+    partly or wholly outside W).  Against the oracle, and (where 512-wide tiles exist,
+    N >= 512) bit for bit against 512-wide tiles: each element sees the same K order."""
     wl = workloads.custom("narrow", T, 128, E, k, N, 1, "none")
     plan, bufs = _full_check(wl, tile_m=256, tile_n=256)
     assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
@@ -288,7 +287,7 @@ def _check_bf16(Y_bf16: np.ndarray, Yref: np.ndarray):
 
 @pytest.mark.parametrize("tile_m,tile_n,N", [(128, 256, 400), (128, 128, 400), (256, 0, 400),
                                             (256, 512, 1040),   # 1040 = 2 x 512 + 16
-                                            (256, 256, 384)])   # a narrow (N=128) last column tile
+                                            (256, 256, 384)])   # a 128-wide last column tile
 def test_bf16_output_full_parity_and_combine(tile_m, tile_n, N):
     wl = workloads.custom("bf16", 1000, 256, 4, 2, N, 2, "none")
     inp = workloads.make_inputs(wl, seed=14)

@@ -148,7 +148,7 @@ def test_grouped_gemm_full_parity(T, d, E, k, N, bias):
 
 @pytest.mark.parametrize("T,E,N,tile_n", [(1000, 2, 400, 0), (1000, 2, 1040, 512),
                                           (1200, 4, 512, 0), (1200, 4, 512, 512),  # ~300-row experts: M=128 tails
-                                          (1000, 2, 1408, 256)])  # a narrow (N=128) last column tile
+                                          (1000, 2, 1408, 256)])  # a 128-wide last column tile
 def test_grouped_gemm_pair_mode(T, E, N, tile_n):
     plan = _grouped_check(T, 128, E, 1, N, "none", tile_m=256, tile_n=tile_n)
     assert plan.info["tile_m"] == 256 and (tile_n == 0 or plan.info["tile_n"] == tile_n)
