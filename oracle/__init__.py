@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     rank_base,
     gather,
     grouped_gemm,
+    grouped_gemm_parallel,
     gemm_entry,
     expert_of_row,
     route,

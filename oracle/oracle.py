@@ -191,6 +191,42 @@ def grouped_gemm(rows_bits: np.ndarray, W_bits: np.ndarray, offsets: np.ndarray)
     return Y
 
 
+def grouped_gemm_parallel(rows_bits: np.ndarray, W_bits: np.ndarray, offsets: np.ndarray,
+                          threads: int):
+    """Step A5 with the output rows split into `threads` contiguous ranges, each
+    computed by the same C function as grouped_gemm in a thread of its own (ctypes
+    releases the GIL for the call).  Every element is the same fp64 sum in the same
+    order, so the result equals grouped_gemm's bit for bit; only the wall time
+    changes.  Used to time the oracle on all host cores."""
+    import concurrent.futures as cf
+
+    rows = np.ascontiguousarray(rows_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    E, d, N = W.shape
+    S = rows.shape[0]
+    Y = np.empty((S, N), np.float64)
+    threads = max(1, min(int(threads), S))
+    bounds = [S * i // threads for i in range(threads + 1)]
+    lib = _load()
+
+    def part(i):
+        r0, r1 = bounds[i], bounds[i + 1]
+        if r1 <= r0:
+            return 0
+        # the part's rows and the expert segments clipped to them, shifted to start at 0
+        sub_off = np.ascontiguousarray(np.clip(off.astype(np.int64) - r0, 0, r1 - r0), dtype=np.int32)
+        sub_rows = rows[r0:r1]
+        out = Y[r0:r1]
+        return lib.oracle_grouped_gemm(_p(sub_rows), _p(W), _p(sub_off), E, d, N, _p(out))
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        rcs = list(ex.map(part, range(threads)))
+    if any(rc != 0 for rc in rcs):
+        raise MemoryError
+    return Y
+
+
 def gemm_entry(row_bits: np.ndarray, We_bits: np.ndarray, n: int) -> float:
     """One element of step A5: row . We[:, n] in fp64."""
     row = np.ascontiguousarray(row_bits, dtype=np.uint16)

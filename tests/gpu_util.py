@@ -71,9 +71,17 @@ def check_Y(Y: np.ndarray, Yref: np.ndarray):
     return float(err.max()), rms
 
 
-def sample_rows_cols(ref, N, tile_m=128, tile_n=256, n_random=48, seed=0):
-    """Rows at every expert's first/last row and tile boundaries, plus random
-    rows; columns at the edges, tile boundaries and random."""
+def sample_rows_cols(ref, N, tile_m=128, tile_n=256, n_random=48, seed=0, row_block=32, col_block=64):
+    """Rows and columns of a sampled check of Y that touches every output tile.
+
+    Rows: every expert's first and last row and the rows on both sides of each
+    tile_m boundary, random rows, and one seeded row inside every block of
+    `row_block` rows of each expert (32: one per epilogue warp's lane quarter of
+    every 128-row tile, so every row tile and both halves of every pair tile).
+    Columns: the edges, the tile_n boundaries, random columns, and one seeded
+    column inside every `col_block` columns (64: one per B box of every column
+    tile).  The check evaluates the whole rows x columns grid, so it holds at
+    least one entry of every (row tile, column tile) pair."""
     rng = np.random.default_rng(seed)
     off = ref["offsets"]
     S = int(off[-1])
@@ -87,28 +95,39 @@ def sample_rows_cols(ref, N, tile_m=128, tile_n=256, n_random=48, seed=0):
     rows = sorted(rows)
     if len(rows) > 96:
         rows = sorted(rng.choice(rows, 96, replace=False).tolist())
-    rows = sorted(set(rows) | set(rng.integers(0, S, n_random).tolist()))
+    rows = set(rows) | set(rng.integers(0, S, n_random).tolist())
+    for e in range(len(off) - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        for r0 in range(a, b, row_block):
+            rows.add(int(rng.integers(r0, min(r0 + row_block, b))))
     cols = {0, N - 1, min(N - 1, tile_n - 1), min(N - 1, tile_n), N // 2}
     cols |= set(rng.integers(0, N, 12).tolist())
-    return rows, sorted(cols)
+    for c0 in range(0, N, col_block):
+        cols.add(int(rng.integers(c0, min(c0 + col_block, N))))
+    return sorted(rows), sorted(cols)
+
+
+def oracle_grid(a_rows_bits, rows, W_dev: torch.Tensor, ref, cols) -> np.ndarray:
+    """The oracle's fp64 Y at rows x cols: one oracle grouped GEMM per expert on that
+    expert's sampled rows (a_rows_bits, gathered in the order of `rows`) and the
+    columns `cols` of its weights."""
+    cols_t = torch.tensor(cols, device=W_dev.device)
+    experts = np.array([oracle.expert_of_row(ref["offsets"], r) for r in rows])
+    want = np.empty((len(rows), len(cols)), np.float64)
+    for e in np.unique(experts):
+        sel = np.nonzero(experts == e)[0]
+        We = workloads.bf16_bits(W_dev[int(e)][:, cols_t])[None]
+        want[sel] = oracle.grouped_gemm(a_rows_bits[sel], We, np.array([0, len(sel)], np.int32))
+    return want
 
 
 def check_Y_sampled(Y_dev: torch.Tensor, x_bits, W_dev: torch.Tensor, ref, k, rows, cols):
-    """Oracle entries one by one at the sampled (row, col) grid."""
+    """Oracle entries at the sampled (row, col) grid."""
     assert not torch.isnan(Y_dev).any().item(), "unwritten (NaN) output rows"
-    perm_sub = ref["perm"][rows]
-    a_rows = oracle.gather(x_bits, perm_sub, k)
-    cols_t = torch.tensor(cols, device=W_dev.device)
+    a_rows = oracle.gather(x_bits, ref["perm"][rows], k)
+    cols_t = torch.tensor(cols, device=Y_dev.device)
     got = Y_dev[torch.tensor(rows, device=Y_dev.device)][:, cols_t].cpu().double().numpy()
-    want = np.empty_like(got)
-    cache = {}
-    for i, row in enumerate(rows):
-        e = oracle.expert_of_row(ref["offsets"], row)
-        if e not in cache:
-            cache[e] = workloads.bf16_bits(W_dev[e][:, cols_t])
-        Wc = cache[e]
-        for j in range(len(cols)):
-            want[i, j] = oracle.gemm_entry(a_rows[i], Wc, j)
+    want = oracle_grid(a_rows, rows, W_dev, ref, cols)
     err = np.abs(got - want)
     rms = float(np.sqrt(np.mean(want ** 2)))
     assert float(err.max()) <= TOL_MAX_REL_RMS * rms, (float(err.max()), rms)

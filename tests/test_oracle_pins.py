@@ -461,3 +461,27 @@ def test_router_logits_order_is_ascending_fma(oracle_mod):
     assert oracle_mod.router_logits(x, W)[0, 0] == 0.0
     bias = np.array([0.5], np.float32)
     assert oracle_mod.router_logits(x, W, bias)[0, 0] == 0.5
+
+
+# ---------------------------------------------------------------- the oracle timed on all host cores
+
+@pytest.mark.parametrize("threads", [2, 5, 8, 64])
+def test_grouped_gemm_on_several_cores_is_bitwise_the_single_threaded_one(oracle_mod, threads):
+    """The benchmark times the oracle's grouped GEMM split by output rows over the
+    host cores.  On the tiny workload (T=256, d=512, E=8, top-2, N=1024) every
+    split gives the single-threaded result bit for bit, and both equal a numpy fp64
+    product of each expert's rows (a cross-check, within fp64 rounding)."""
+    from moe_token_dispatch_route_gb300 import workloads
+    wl = workloads.WORKLOADS["tiny"]
+    inp = workloads.make_inputs(wl, seed=0)
+    ref = oracle_mod.route(inp["logits"].numpy(), wl.k)
+    rows = oracle_mod.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+    Wb = workloads.bf16_bits(inp["W"])
+    one = oracle_mod.grouped_gemm(rows, Wb, ref["offsets"])
+    many = oracle_mod.grouped_gemm_parallel(rows, Wb, ref["offsets"], threads)
+    assert np.array_equal(one.view(np.uint64), many.view(np.uint64))
+    off = ref["offsets"]
+    for e in range(wl.E):
+        a, b = int(off[e]), int(off[e + 1])
+        want = _bits_to_f64(rows[a:b]) @ _bits_to_f64(Wb[e])
+        assert np.allclose(many[a:b], want, rtol=1e-12, atol=1e-12)

@@ -4,7 +4,9 @@ that owns all device memory).  It keeps its scratch in a static device array
 inside the library instead of a caller workspace.
 
 Checked through the C ABI against moe_route (the workspace entry point) on
-the same inputs, for two calls in a row with different inputs, so that
+the same inputs, bit for bit (the two run the same kernels), and against the
+CPU oracle (indices, counts, offsets, permutation and inverse bit-exact,
+gates within 1e-5), for two calls in a row with different inputs, so that
 leftovers of the first call in the shared array cannot go unnoticed.  This
 file is collected last on purpose.
 """
@@ -12,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
 from tests.gpu_util import TOL_GATE
 
@@ -42,7 +45,8 @@ def test_noalloc_route_matches_workspace_route_twice(name, route_flags):
     plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, route_flags=route_flags)
     ws = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
     for call, seed in enumerate((11, 12)):
-        logits = workloads.make_inputs(wl, seed=seed, with_weights=False)["logits"].to(dev)
+        logits_h = workloads.make_inputs(wl, seed=seed, with_weights=False)["logits"]
+        logits = logits_h.to(dev)
         want = _outputs(plan, dev)
         binding.moe_route(plan, logits, *_args(want), ws)
         got = _outputs(plan, dev)
@@ -50,8 +54,15 @@ def test_noalloc_route_matches_workspace_route_twice(name, route_flags):
         torch.cuda.synchronize()
         for key in KEYS:
             assert torch.equal(got[key], want[key]), f"call {call}: {key}"
-        err = (got["topk_w"].double() - want["topk_w"].double()).abs().max().item()
-        assert err <= TOL_GATE, f"call {call}: gate weights differ by {err}"
+        # the same kernels on the same logits: the gates agree bit for bit too
+        assert torch.equal(got["topk_w"].view(torch.int32), want["topk_w"].view(torch.int32)), \
+            f"call {call}: gate weights differ from moe_route"
+        ref = oracle.route(logits_h.numpy(), wl.k, renorm=bool(route_flags & binding.MOE_ROUTE_RENORM))
+        for key in KEYS:
+            g = got[key].cpu().numpy().reshape(ref[key].shape)
+            assert np.array_equal(g, ref[key]), f"call {call}: {key} differs from the oracle"
+        err = float(np.abs(got["topk_w"].cpu().double().numpy() - ref["topk_w"]).max())
+        assert err <= TOL_GATE, f"call {call}: gate weights differ from the oracle by {err}"
 
 
 def test_noalloc_route_rejects_plans_beyond_its_scratch():
