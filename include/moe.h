@@ -36,8 +36,10 @@
  *    caller's `dev_status` buffer and read later with moe_read_status.  No
  *    kernel traps.
  *  - Shape limits: 1 <= E <= 1024; 1 <= k <= min(E, 32); 0 <= T; T*k < 2^31;
- *    d % 64 == 0 and 64 <= d <= 65536; N % 16 == 0 and 16 <= N; E % R == 0
- *    and 1 <= R <= 32.  Outside them: MOE_ERR_UNSUPPORTED.
+ *    d % 16 == 0 and 16 <= d <= 65536; N % 16 == 0 and 16 <= N; E % R == 0
+ *    and 1 <= R <= 32.  Outside them: MOE_ERR_UNSUPPORTED.  (A reduction d
+ *    that is not a multiple of 64 ends in a shorter last k-block: its MMAs
+ *    stop at d.)
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -222,6 +224,33 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
                                void* workspace, int32_t* dev_status, void* stream);
 
 /*
+ * moe_dispatch_gemm_combine -- moe_dispatch_gemm with the combine step (the
+ * reverse exchange that the "MoE Dispatch + GEMM" row of the articles' table
+ * of fused kernels implies after the per-expert GEMM) fused into the GEMM's
+ * epilogue: instead of writing Y, each destination row i, times the gate of
+ * its slot s = perm[i], is added into its token's output row:
+ *   out[t][n] = sum_{j<k} topk_w[t][j] * (x[t] . W[topk_idx[t][j]][:, n]),
+ * each product rounded to fp32 and added with fp32 reductions in global
+ * memory (no Y round trip, no separate combine launch).  For k <= 2 the
+ * result does not depend on the order in which the two reductions land (a
+ * two-term fp32 sum into a zeroed row is commutative), so it is the same on
+ * every run, role split and grid size; it differs from moe_combine's
+ * fused multiply-adds by at most the rounding of one product.
+ *   topk_w in:  fp32 [T][k] from moe_route (device).
+ *   out    out: fp32 [T][N], 16-byte aligned.  The call zeroes it
+ *               (cudaMemsetAsync on `stream`) before its launch.
+ * Other arguments as for moe_dispatch_gemm (the receive buffers are written;
+ * no Y is written whatever the plan's out_dtype).  MOE_ERR_UNSUPPORTED for
+ * k > 2, where the reductions' order would change the bits: use
+ * moe_dispatch_gemm + moe_combine there.  Launches a memset and one kernel.
+ */
+MOE_API moe_status_t moe_dispatch_gemm_combine(moe_plan_t plan, const uint16_t* x,
+                                       const int32_t* offsets, const int32_t* perm,
+                                       const float* topk_w, const uint16_t* W,
+                                       void* const* recv, float* out, void* workspace,
+                                       int32_t* dev_status, void* stream);
+
+/*
  * moe_dispatch_gemm_swiglu -- moe_dispatch_gemm for a gated (SwiGLU) expert
  * up-projection.  The plan's N is 2F: W1's first F columns are the gate
  * projection and the last F the up projection.  Each GEMM tile computes the
@@ -347,7 +376,8 @@ MOE_API moe_status_t moe_read_status(const int32_t* dev_status, void* stream, in
  *    before any launch.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  A lookup that fails returns MOE_ERR_CUDA and
+ *    is tried again by the next call on that device.
  *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    routine.  It clears the ticket counter with cudaMemsetAsync on `stream`
  *    before its launch; the count table is fully rewritten by every call.

@@ -67,7 +67,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTED = ("moe_plan", "moe_plan_destroy", "moe_plan_info", "moe_route", "moe_dispatch_gemm",
             "moe_read_status", "moe_status_string", "moe_route_noalloc", "moe_combine",
             "moe_router_logits", "moe_route_biased", "moe_dispatch_gemm_swiglu",
-            "moe_grouped_gemm", "moe_gather_gemm", "moe_set_trace")
+            "moe_grouped_gemm", "moe_gather_gemm", "moe_set_trace", "moe_dispatch_gemm_combine")
 
 
 def load_library(path: str = LIB_PATH):
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_biased.restype = I32
     lib.moe_dispatch_gemm.argtypes = [VP] * 10
     lib.moe_dispatch_gemm.restype = I32
+    lib.moe_dispatch_gemm_combine.argtypes = [VP] * 11
+    lib.moe_dispatch_gemm_combine.restype = I32
     lib.moe_dispatch_gemm_swiglu.argtypes = [VP] * 10
     lib.moe_dispatch_gemm_swiglu.restype = I32
     lib.moe_grouped_gemm.argtypes = [VP] * 8
@@ -206,6 +208,22 @@ def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, worksp
                                           _ptr(workspace), _ptr(dev_status),
                                           _stream(stream, plan.device))
     _check(rc, "moe_dispatch_gemm")
+
+
+def moe_dispatch_gemm_combine(plan: Plan, x, offsets, perm, topk_w, W, recv: Sequence, out, workspace,
+                              dev_status, stream=None) -> None:
+    """Fused dispatch + grouped GEMM + combine (k <= 2): out[t] = sum_j w[t,j] * (x[t] W[e_j])."""
+    arr = (ctypes.c_void_p * max(1, len(recv)))(*[_ptr(r) for r in recv])
+    rc = load_library().moe_dispatch_gemm_combine(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm),
+                                                  _ptr(topk_w), _ptr(W), ctypes.cast(arr, ctypes.c_void_p),
+                                                  _ptr(out), _ptr(workspace), _ptr(dev_status),
+                                                  _stream(stream, plan.device))
+    _check(rc, "moe_dispatch_gemm_combine")
+
+
+def dispatch_gemm_combine(plan: Plan, x, W, bufs: "MoeBuffers", out, stream=None):
+    moe_dispatch_gemm_combine(plan, x, bufs.offsets, bufs.perm, bufs.topk_w, W, bufs.recv, out,
+                              bufs.workspace, bufs.status, stream)
 
 
 def moe_dispatch_gemm_swiglu(plan: Plan, x, offsets, perm, W1, recv: Sequence, H, workspace,

@@ -59,6 +59,8 @@ struct TileInfo {
     int arow;  // first row inside the rank's receive buffer
     int m128;  // CTA pairs: 1 for an expert's last tile of at most 128 rows, run as an
                // M=128 pair MMA (64 rows per CTA); 0 otherwise
+    int narrow;  // CTA pairs, 256-wide tiles: 1 for a last column tile of at most 128
+                 // columns, run as an N=128 pair MMA; 0 otherwise
 };
 
 constexpr int kMaxPieceBufs = 8;
@@ -488,6 +490,52 @@ __device__ __forceinline__ void store_block_rows(float* tile, const uint32_t (&v
     __syncwarp();
 }
 
+// Combine epilogue: the same transposed block, each row scaled by its slot's gate and
+// added into its token's row of `out` with 16-byte fp32 reductions (red.global.add).
+// `col0`: Y column of the block's column 0; `tok_lane` / `w_lane`: token and gate of
+// the block's row `lane`.  With at most two slots per token the two reductions into a
+// zeroed row give fl(a + b) in either order, so the result does not depend on timing.
+__device__ __forceinline__ void red_block_rows(float* tile, const uint32_t (&v)[32], float* out, size_t ld,
+                                               int col0, int rows_valid, int cols_valid, int lane,
+                                               int tok_lane, float w_lane) {
+    float4* mine = reinterpret_cast<float4*>(tile + lane * kEpiStride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        mine[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                              __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+    __syncwarp();
+    const int sub = lane >> 3;
+    const int col = (lane & 7) * 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int row = 4 * j + sub;
+        const int t = __shfl_sync(kFull, tok_lane, row);
+        const float w = __shfl_sync(kFull, w_lane, row);
+        if (row < rows_valid && col < cols_valid) {
+            float4 y = *reinterpret_cast<const float4*>(tile + row * kEpiStride + col);
+            y.x *= w;
+            y.y *= w;
+            y.z *= w;
+            y.w *= w;
+            atomicAdd(reinterpret_cast<float4*>(out + (size_t)t * ld + col0 + col), y);
+        }
+    }
+    __syncwarp();
+}
+
+// Combine: token and gate of tile row `r` (lane's row of the warp's block), or (0, 0)
+// past the tile's rows.
+__device__ __forceinline__ void combine_row(const DispatchGemmParams& p, int row0, int r, int rows,
+                                            int& tok, float& w) {
+    tok = 0;
+    w = 0.f;
+    if (r < rows) {
+        const int s = __ldg(p.perm + row0 + r);
+        tok = s / p.k;
+        w = __ldg(p.topk_w + s);
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x = lo: the lower address
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -545,6 +593,18 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
                 store_block_rows(epi, w, reinterpret_cast<float*>(ybase + c), (size_t)p.N / 2, rows_valid,
                                  (ncols - c) / 2, lane);
         }
+    } else if (p.combine) {
+        const int ncols = min(bn, p.N - ti.n * bn);
+        int tok;
+        float w;
+        combine_row(p, ti.row0, 32 * q + lane, ti.rows, tok, w);
+        for (int c = 0; c < ncols; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32(tbase + (uint32_t)c, v);
+            tmem_ld_wait(v);
+            if (rows_valid > 0)
+                red_block_rows(epi, v, p.out, (size_t)p.N, ti.n * bn + c, rows_valid, ncols - c, lane, tok, w);
+        }
     } else {
         float* ybase = static_cast<float*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
         const int ncols = min(bn, p.N - ti.n * bn);
@@ -571,6 +631,9 @@ __device__ __forceinline__ void epilogue_tile_m128(const DispatchGemmParams& p, 
     if (rows_valid <= 0) return;  // warp-uniform
     const uint32_t tq = tacc + ((uint32_t)(32 * q) << 16);
     const size_t row = (size_t)(ti.row0 + 32 * rb);
+    int tok = 0;
+    float wgt = 0.f;
+    if (p.combine) combine_row(p, ti.row0, 32 * rb + lane, ti.rows, tok, wgt);
     for (int h = 0; h < bn / 256; ++h) {
         const int col0 = ti.n * bn + 256 * h + 128 * ch;  // first Y column of this warp's block
         const int ncols = min(128, p.N - col0);
@@ -591,6 +654,13 @@ __device__ __forceinline__ void epilogue_tile_m128(const DispatchGemmParams& p, 
                 }
                 store_block_rows(epi, w, reinterpret_cast<float*>(ybase + c), (size_t)p.N / 2, rows_valid,
                                  (ncols - c) / 2, lane);
+            }
+        } else if (p.combine) {
+            for (int c = 0; c < ncols; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32(t0 + (uint32_t)c, v);
+                tmem_ld_wait(v);
+                red_block_rows(epi, v, p.out, (size_t)p.N, col0 + c, rows_valid, ncols - c, lane, tok, wgt);
             }
         } else {
             float* ybase = static_cast<float*>(p.Y) + row * p.N + col0;
@@ -663,7 +733,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
         const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
         if (tile >= total_tiles) {
-            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = 0;
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = ti.narrow = 0;
             ti.rows = -1;
         } else {
             const int u = (int)(tile / (uint32_t)p.n_tiles);
@@ -688,6 +758,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             ti.rank = e / e_per_rank;
             ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
             ti.m128 = 0;
+            ti.narrow = 0;
         }
         ctl->ring[slot] = ti;
         mbar_arrive(smem_addr(&ctl->sfull[slot]));
@@ -788,8 +859,12 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+            // the last k-block of a reduction that is not a multiple of 64 stops at d: the
+            // loaded columns past d (zero-filled A, the next expert's W rows) are not used
+            const int ksteps = kb == p.k_blocks - 1 ? p.last_ksteps : kTileK / kUmmaK;
 #pragma unroll
             for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                if (kk >= ksteps) break;
                 // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
                 // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
                 //    1024 B apart (SBO); K step of 16 rows = +2048 B.
@@ -925,13 +1000,16 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
                 break;
             }
             const uint32_t a0 = smem_addr(sA + stage * kABytes);
-            const size_t kofs = (size_t)kb * (kTileK * 2) + 16 * c;
+            // this lane's 8 columns start at kb * 64 + 8 c; past d (a last k-block of a
+            // reduction that is not a multiple of 64) nothing is read and zeros are written
+            const bool in_row = kb * kTileK + 8 * c < p.d;
+            const size_t kofs = in_row ? (size_t)kb * (kTileK * 2) + 16 * c : 0;
 #pragma unroll
             for (int i = 0; i < kIters; ++i) {
                 const int r = r0 + 4 * i + (lane >> 3);
                 const int t = tok[i];
                 cp_async16_cg_zfill(a0 + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4),
-                                    xb + (size_t)(t < 0 ? 0 : t) * row_bytes + kofs, t < 0 ? 0 : 16);
+                                    xb + (size_t)(t < 0 ? 0 : t) * row_bytes + kofs, (t < 0 || !in_row) ? 0 : 16);
             }
             cp_async_commit();
             int tail = head + npend;
@@ -1088,6 +1166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * An expert's last tile of at most 128 rows runs as an M=128 pair MMA, 64
 //    rows per CTA, both CTAs waiting for that one row tile's flag
 //    (pair_half_info, epilogue_tile_m128).
+//  * With 256-wide tiles, a last column tile of at most 128 columns (N not a
+//    multiple of 256) runs as an N=128 pair MMA: each CTA loads one 64-column
+//    B box instead of two, and the MMA does half the work.  Not for M=128 or
+//    gated tiles.
 // The scatter role is unchanged; a pair takes one role ticket and its two
 // CTAs become scatter CTAs 2t and 2t+1.
 template <int STAGES, int BN>
@@ -1100,6 +1182,7 @@ struct PairCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 256);
     static constexpr uint32_t kIdesc128 = idesc_bf16_f32_kmajA_mnmajB(kTileM, 256);  // tail tiles
+    static constexpr uint32_t kIdescN128 = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 128);  // narrow tiles
     static constexpr int kTmemCols = 512;                // two 256-column accumulators or one of 512
     static constexpr int kAccs = 512 / BN;               // accumulators (TMEM double buffer for 256)
     static constexpr size_t kSmem =
@@ -1115,7 +1198,12 @@ struct PairCfg {
 // Tile description of one CTA's half of a pair tile.  An expert's last pair tile
 // with at most 128 rows runs as an M=128 pair MMA (not in gated mode): each CTA
 // holds 64 of its rows (rows [64 half, 64 half + 64) of the 128-row tile 2 m2),
-// and both halves wait for that row tile's flag.
+// and both halves wait for that row tile's flag.  Each CTA still loads a whole
+// 128-row A box (the rank buffer's one tensor map): the box's rows 64-127 lie
+// past this CTA's 64 rows (the peer's rows, the next expert's rows that the
+// scatter may still be writing, or rows past the buffer, zero-filled).  The
+// M=128 MMA reads only rows 0-63 of each CTA's A tile, so those extra rows are
+// never used and a race on them cannot change a result.
 __device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, int e, int m2,
                                int n, int half, TileInfo& ti) {
     const int e_per_rank = p.E / p.R;
@@ -1169,6 +1257,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             TileInfo other;
             if (tile >= total_tiles) {
                 ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = 0;
+                ti.narrow = 0;
                 ti.e = -1;
                 other = ti;
             } else {
@@ -1180,6 +1269,8 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 const int m2 = local % pt_e;
                 pair_half_info(p, mt_base, e, m2, n, 0, ti);
                 pair_half_info(p, mt_base, e, m2, n, 1, other);
+                ti.narrow = other.narrow =
+                    (BN == 256 && !p.glu && !ti.m128 && p.N - n * BN <= BN / 2) ? 1 : 0;
             }
             ctl->ring[slot] = ti;
             const int* o = reinterpret_cast<const int*>(&other);
@@ -1234,6 +1325,10 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
             for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, cur.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
+        // a narrow tile (N=128 MMA): each CTA holds 64 of its 128 columns, box 0 or 1
+        const int nbox = cur.narrow ? 1 : 2 * C::kHalves;
+        if (cur.narrow) bcol[0] = b_box_col(p, cur.n, C::kBN, leader ? 0 : 1);
+        const uint32_t stage_tx = 2u * (uint32_t)(C::kABytes + 8192 * nbox);  // both CTAs' bytes
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -1252,12 +1347,13 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             }
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
-            if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
+            if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
             tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
 #pragma unroll
             for (int b = 0; b < 2 * C::kHalves; ++b)
-                tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
-                                 brow + kb * kTileK);
+                if (b < nbox)
+                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                     brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -1294,7 +1390,8 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     while (ok) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 25, true, true)) break;
         const int e = ctl->ring[slot].e;
-        const uint32_t idesc = ctl->ring[slot].m128 ? C::kIdesc128 : C::kIdesc;
+        const uint32_t idesc =
+            ctl->ring[slot].m128 ? C::kIdesc128 : ctl->ring[slot].narrow ? C::kIdescN128 : C::kIdesc;
         mbar_arrive(smem_addr(&ctl->sempty[slot]));
         if (++slot == kRing) {
             slot = 0;
@@ -1312,8 +1409,10 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+            const int ksteps = kb == p.k_blocks - 1 ? p.last_ksteps : kTileK / kUmmaK;  // stop at d
 #pragma unroll
             for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                if (kk >= ksteps) break;
                 const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)

@@ -105,7 +105,7 @@ moe_status_t validate_shape(const moe_shape_t& s) {
         return MOE_ERR_INVALID_ARG;
     const int R = s.num_ranks == 0 ? 1 : s.num_ranks;
     if (s.E > kMaxE || s.k > std::min(s.E, 32)) return MOE_ERR_UNSUPPORTED;
-    if (s.d % kTileK != 0 || s.d > 65536) return MOE_ERR_UNSUPPORTED;
+    if (s.d % kUmmaK != 0 || s.d > 65536) return MOE_ERR_UNSUPPORTED;  // whole K=16 MMA steps
     if (s.N % 16 != 0) return MOE_ERR_UNSUPPORTED;
     if (R > kMaxRanks || s.E % R != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s.T * s.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -339,22 +339,29 @@ moe_status_t moe_route_biased(moe_plan_t plan, const float* logits, const float*
 
 namespace {
 
-enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped, kGather };
+enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped, kGather, kDispatchCombine };
 
 // The three entry points that run the persistent GEMM kernel.  kDispatch and
 // kDispatchSwiglu scatter x into the receive buffers and compute on the rows
 // as they land; kGrouped computes on rows the caller has already laid out.
 moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const int32_t* offsets,
                       const int32_t* perm, const uint16_t* W, void* const* recv, const uint16_t* A,
-                      void* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream) {
+                      void* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream,
+                      const float* topk_w = nullptr, float* out = nullptr) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
     const bool glu = mode == GemmMode::kDispatchSwiglu;
+    const bool combine = mode == GemmMode::kDispatchCombine;
     if (glu && plan->tile_n == 192) return MOE_ERR_UNSUPPORTED;  // halves must be whole 64-column boxes
+    if (combine && plan->k > 2) return MOE_ERR_UNSUPPORTED;      // reproducible for k <= 2 only
     if (plan->T == 0) return MOE_OK;
     if (!offsets || !W || !aligned(W, 16) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
-    if (glu ? (!H || !aligned(H, 16)) : (!Y || !aligned(Y, 16))) return MOE_ERR_INVALID_ARG;
+    if (combine) {
+        if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    } else if (glu ? (!H || !aligned(H, 16)) : (!Y || !aligned(Y, 16))) {
+        return MOE_ERR_INVALID_ARG;
+    }
     const bool grouped = mode == GemmMode::kGrouped;
     const bool gather = mode == GemmMode::kGather;
     const int nA = grouped ? 1 : gather ? 0 : plan->R;  // A tensor maps (the gather has none)
@@ -405,7 +412,10 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     if (!grouped && !gather)  // the gather mode has no receive buffers (recv may be NULL)
         for (int r = 0; r < plan->R; ++r) prm.recv[r] = static_cast<uint16_t*>(recv[r]);
     prm.Y = Y;
-    prm.out_bf16 = plan->shape.out_dtype == MOE_OUT_BF16 ? 1 : 0;
+    prm.out_bf16 = (!combine && plan->shape.out_dtype == MOE_OUT_BF16) ? 1 : 0;
+    prm.combine = combine ? 1 : 0;
+    prm.topk_w = topk_w;
+    prm.out = out;
     prm.trace = plan->trace;
     prm.H = H;
     prm.glu = glu ? 1 : 0;
@@ -428,12 +438,19 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     const int tile_cols = glu ? plan->tile_n / 2 : plan->tile_n;  // output columns per tile
     const int out_cols = glu ? plan->N / 2 : plan->N;
     prm.n_tiles = (out_cols + tile_cols - 1) / tile_cols;
-    prm.k_blocks = plan->d / kTileK;
+    prm.k_blocks = (plan->d + kTileK - 1) / kTileK;
+    prm.last_ksteps = (plan->d - kTileK * (prm.k_blocks - 1)) / kUmmaK;
     prm.producer_ctas = (grouped || gather) ? 0 : plan->producer_ctas;
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
     cudaError_t lerr;
+    if (combine &&
+        cudaMemsetAsync(out, 0, (size_t)plan->T * plan->N * sizeof(float), static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
     if (gather && plan->pair) {
         // the direct gather runs in the single-CTA kernel: 256-wide tiles, 4 stages
         const size_t smem = dispatch_gemm_smem_bytes(256, 4);
@@ -474,6 +491,14 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
                                void* workspace, int32_t* dev_status, void* stream) {
     return run_gemm(plan, GemmMode::kDispatch, x, offsets, perm, W, recv, nullptr, Y, nullptr,
                     workspace, dev_status, stream);
+}
+
+moe_status_t moe_dispatch_gemm_combine(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
+                                       const int32_t* perm, const float* topk_w, const uint16_t* W,
+                                       void* const* recv, float* out, void* workspace, int32_t* dev_status,
+                                       void* stream) {
+    return run_gemm(plan, GemmMode::kDispatchCombine, x, offsets, perm, W, recv, nullptr, nullptr, nullptr,
+                    workspace, dev_status, stream, topk_w, out);
 }
 
 moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,

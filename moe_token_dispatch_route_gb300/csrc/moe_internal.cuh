@@ -91,7 +91,8 @@ struct DispatchGemmParams {
     int32_t* status;
     long long timeout_ns;
     int T, d, E, k, N, R, cap;
-    int tile_n, n_tiles, k_blocks;
+    int tile_n, n_tiles, k_blocks;  // k_blocks = ceil(d / 64)
+    int last_ksteps;                // K=16 MMA steps in the last k-block: (d - 64 (k_blocks - 1)) / 16
     int producer_ctas;
     int max_mtiles;                 // size of flags[] and chunk_cnt[]
     int skip_publish;               // m-tile whose flag is never published, or -1
@@ -103,6 +104,10 @@ struct DispatchGemmParams {
     int gather;                     // 1: A rows are copied from x by perm into shared memory
                                     //    (no receive buffers, no scatter, no flags)
     int out_bf16;                   // 1: Y is bf16 (fp32 accumulator rounded once)
+    int combine;                    // 1: no Y; each row, times its slot's gate, is added into
+                                    //    its token's row of `out` (zeroed before the launch)
+    const float* topk_w;            // combine: [T*k] gate of each slot
+    float* out;                     // combine: fp32 [T][N]
     unsigned long long* trace;      // [grid][kTraceWords] per-CTA stamps, or null (off)
 };
 

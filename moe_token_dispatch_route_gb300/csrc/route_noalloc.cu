@@ -27,25 +27,26 @@ constexpr int kMaxDevices = 64;
 // its launch.  Calls share it, so calls that overlap on the GPU race.
 static __device__ __align__(256) int32_t g_route_scratch[kHeaderInts + kTableInts];
 
-// Device address of g_route_scratch, looked up once per device with that device
-// current.  In host code the symbol itself is only a host-side stand-in.
+// Device address of g_route_scratch, looked up with that device current.  In
+// host code the symbol itself is only a host-side stand-in.  Only a successful
+// lookup is kept: a failed one (a transient error, or a first call made during a
+// stream capture) is retried by the next call on that device.
 struct ScratchSlot {
-    std::once_flag once;
+    std::mutex mu;
     void* ptr = nullptr;
-    cudaError_t err = cudaErrorNotReady;
 };
 ScratchSlot g_slots[kMaxDevices];
 
 void* scratch_address(int device) {
     if (device < 0 || device >= kMaxDevices) return nullptr;
     ScratchSlot& s = g_slots[device];
-    std::call_once(s.once, [&s] {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.ptr) {
         void* p = nullptr;
-        s.err = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (s.err == cudaSuccess) s.ptr = p;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) == cudaSuccess) s.ptr = p;
         else cudaGetLastError();
-    });
-    return s.err == cudaSuccess ? s.ptr : nullptr;
+    }
+    return s.ptr;
 }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

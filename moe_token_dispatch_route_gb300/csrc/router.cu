@@ -23,7 +23,7 @@
 //          batches and few experts, where the work is a few warps per SM and the
 //          time goes to the chains' latency and the per-chunk barriers.
 //
-// Fallback kernel (any E, 4-byte aligned x): a block computes TB tokens x EB
+// Fallback kernel (any E, d a multiple of 16, 4-byte aligned x): a block computes TB tokens x EB
 // experts; each thread owns one expert and P tokens (every TB/P-th token, so the
 // token groups of one warp read adjacent rows) with P accumulators, P chosen so the
 // grid fills the GPU; the next chunk is loaded into registers while the current
@@ -69,13 +69,14 @@ __global__ void __launch_bounds__(kRtThreads) router_logits_kernel(const RouterA
         for (int u = 0; u < XPER; ++u) {
             const int idx = tid + u * kRtThreads;
             const int t = t0 + idx / kRtChunk;
-            xr[u] = t < a.T ? __ldg(a.x + (size_t)t * a.d + i0 + idx % kRtChunk) : (uint16_t)0;
+            const int i = i0 + idx % kRtChunk;
+            xr[u] = (t < a.T && i < a.d) ? __ldg(a.x + (size_t)t * a.d + i) : (uint16_t)0;
         }
 #pragma unroll
         for (int u = 0; u < WPER; ++u) {
             const int idx = tid + u * kRtThreads;
             const int ee = idx % EB;
-            wr[u] = (idx < kRtChunk * EB && e0 + ee < a.E)
+            wr[u] = (idx < kRtChunk * EB && e0 + ee < a.E && i0 + idx / EB < a.d)
                         ? __ldg(a.Wr + (size_t)(i0 + idx / EB) * a.E + e0 + ee) : (uint16_t)0;
         }
     };
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kRtThreads) router_logits_kernel(const RouterA
         if (i0 + kRtChunk < a.d) load_chunk(i0 + kRtChunk);
 #pragma unroll
         for (int ii = 0; ii < kRtChunk; ii += 4) {
+            if (i0 + ii >= a.d) break;  // a last chunk of 16 (d % 32 == 16): no step past d
             const float w0 = Ws[ii][eloc], w1 = Ws[ii + 1][eloc], w2 = Ws[ii + 2][eloc], w3 = Ws[ii + 3][eloc];
 #pragma unroll
             for (int q = 0; q < P; ++q) {
@@ -306,7 +308,7 @@ cudaError_t router_prepare_attributes() {
 
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
-    if (a.d % kRtChunk != 0) return cudaErrorInvalidValue;
+    if (a.d % 16 != 0) return cudaErrorInvalidValue;
     const bool streamed = a.E % 8 == 0 && a.d % 64 == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
                           (reinterpret_cast<uintptr_t>(a.Wr) & 15) == 0;
     if (streamed) {

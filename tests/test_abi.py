@@ -78,6 +78,8 @@ def _plan_rc(lib, **kw):
     (dict(E=8, k=9), binding.MOE_ERR_UNSUPPORTED),
     (dict(E=64, k=33), binding.MOE_ERR_UNSUPPORTED),
     (dict(d=100), binding.MOE_ERR_UNSUPPORTED),
+    (dict(d=72), binding.MOE_ERR_UNSUPPORTED),                     # d % 16 != 0
+    (dict(d=65536 + 16), binding.MOE_ERR_UNSUPPORTED),
     (dict(d=65536 + 64), binding.MOE_ERR_UNSUPPORTED),
     (dict(N=24), binding.MOE_ERR_UNSUPPORTED),
     (dict(num_ranks=3), binding.MOE_ERR_UNSUPPORTED),

@@ -6,7 +6,8 @@ import torch
 
 import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
-from tests.gpu_util import TOL_FRO, TOL_MAX_REL_RMS, check_Y, run_path
+from tests.gpu_util import (TOL_FRO, TOL_MAX_REL_RMS, check_recv, check_route, check_Y, oracle_grid, run_path,
+                            sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,3 +77,99 @@ def test_combine_is_repeatable_bitwise():
     a = _combine_gpu(plan, bufs, wl.T, wl.N)
     b = _combine_gpu(plan, bufs, wl.T, wl.N)
     assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ combine fused into the GEMM epilogue
+
+def _fused(wl, inp, **plan_kw):
+    """route + moe_dispatch_gemm_combine; receive buffers and the output poisoned first
+    (the call zeroes `out` itself)."""
+    dev = torch.device("cuda")
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **plan_kw)
+    bufs = binding.MoeBuffers(plan, dev)
+    for r in bufs.recv:
+        r.fill_(float("nan"))
+    out = torch.full((wl.T, wl.N), float("nan"), dtype=torch.float32, device=dev)
+    W = inp["W"] if inp["W"].device.type == "cuda" else inp["W"].to(dev)
+    binding.route(plan, inp["logits"].to(dev), bufs)
+    binding.dispatch_gemm_combine(plan, inp["x"].to(dev), W, bufs, out)
+    rc, status = binding.moe_read_status(bufs.status)
+    return plan, bufs, out, rc, status
+
+
+@pytest.mark.parametrize("T,d,E,k,N,R,tile_m,tile_n", [
+    (256, 512, 8, 2, 1024, 1, 0, 0),        # the tiny workload's shape, single-CTA tiles
+    (900, 128, 4, 1, 512, 1, 0, 0),         # k = 1: one reduction per output element
+    (1200, 128, 4, 2, 1408, 2, 256, 256),   # CTA pairs: M=128 tails, an N=128 last column tile
+    (1000, 128, 2, 2, 1040, 1, 256, 512),   # 512-wide pair tiles with a 16-wide tail
+    (600, 80, 8, 2, 272, 1, 128, 128),      # d = 80; 128-wide single tiles, ragged column tail
+    (64, 256, 128, 2, 256, 1, 0, 0),        # decode-like: many experts with 1-3 rows
+])
+def test_fused_combine_full_parity(T, d, E, k, N, R, tile_m, tile_n):
+    wl = workloads.custom("fcomb", T, d, E, k, N, R)
+    inp = workloads.make_inputs(wl, seed=16)
+    plan, bufs, out, rc, st = _fused(wl, inp, tile_m=tile_m, tile_n=tile_n)
+    assert rc == 0, st
+    if tile_m:
+        assert plan.info["tile_m"] == tile_m
+    ref = oracle.route(inp["logits"].numpy(), k)
+    check_route(bufs, ref, k)
+    xb = workloads.bf16_bits(inp["x"])
+    rows = oracle.gather(xb, ref["perm"], k)
+    check_recv(bufs, xb, ref, k, R, rows)
+    Yref = oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"])
+    check_Y(out.cpu().double().numpy(), oracle.combine(Yref, ref["topk_w"], ref["dest"]))
+
+
+def test_fused_combine_is_bitwise_repeatable_across_role_splits_and_grids():
+    """k = 2: the two gate-weighted rows of a token reach a zeroed output row in an
+    order that depends on timing, and fl(a + b) = fl(b + a): every split and grid size
+    (and a second call) gives the same bits."""
+    wl = workloads.custom("fcsplit", 1500, 256, 8, 2, 640, 2, "none")
+    inp = workloads.make_inputs(wl, seed=17)
+    for tile_m in (128, 256):
+        outs = []
+        for kw in (dict(), dict(producer_ctas=2), dict(num_ctas=16, producer_ctas=4), dict(num_ctas=2)):
+            for _ in range(2):
+                _, _, out, rc, st = _fused(wl, inp, tile_m=tile_m, **kw)
+                assert rc == 0, st
+                outs.append(out)
+        for o in outs[1:]:
+            assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
+
+
+def test_fused_combine_refuses_more_than_two_slots():
+    wl = workloads.custom("fck4", 100, 64, 8, 4, 128)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N)
+    bufs = binding.MoeBuffers(plan, "cuda")
+    out = torch.zeros(wl.T, wl.N, device="cuda")
+    with pytest.raises(binding.MoeError) as exc:
+        binding.dispatch_gemm_combine(plan, torch.zeros(wl.T, wl.d, dtype=torch.bfloat16, device="cuda"),
+                                      torch.zeros(wl.E, wl.d, wl.N, dtype=torch.bfloat16, device="cuda"),
+                                      bufs, out)
+    assert exc.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
+def test_fused_combine_mixtral_full_size_sampled():
+    """The Mixtral-shaped layer in the benchmark's launch configuration: every output
+    element written (poisoned first), and sampled tokens whose slots fall in every
+    (row tile, column tile) of the GEMM against the oracle's combine."""
+    wl = workloads.WORKLOADS["mixtral"]
+    inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
+    plan, bufs, out, rc, st = _fused(wl, inp)
+    assert rc == 0, st
+    assert not torch.isnan(out).any().item(), "unwritten output"
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    rows, cols = sample_rows_cols(ref, wl.N, tile_n=plan.info["tile_n"], n_random=16)
+    toks = sorted({int(ref["perm"][r]) // wl.k for r in rows})
+    # both slots of every sampled token, as destination rows, and the oracle's Y there
+    slots = np.array([t * wl.k + j for t in toks for j in range(wl.k)])
+    drows = [int(ref["dest"][s]) for s in slots]
+    a_rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"][drows], wl.k)
+    Ysub = oracle_grid(a_rows, drows, inp["W"], ref, cols)
+    want = oracle.combine(Ysub, ref["topk_w"][toks], np.arange(len(slots), dtype=np.int32))
+    got = out[torch.tensor(toks, device="cuda")][:, torch.tensor(cols, device="cuda")].cpu().double().numpy()
+    err = np.abs(got - want)
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    assert float(err.max()) <= TOL_MAX_REL_RMS * rms, (float(err.max()), rms)
+    assert float(np.linalg.norm(got - want)) <= TOL_FRO * float(np.linalg.norm(want))

@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
-from tests.gpu_util import check_recv, check_route, check_Y, check_Y_sampled, run_path, sample_rows_cols
+from tests.gpu_util import (check_recv, check_route, check_Y, check_Y_sampled, oracle_grid, run_path,
+                            sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +52,15 @@ def test_edge_shapes_full_parity(T, d, E, k, N, R, bias):
 @pytest.mark.parametrize("tile_n", [128, 192, 256])
 def test_tile_widths(tile_n):
     _full_check(workloads.custom("tn", 700, 256, 8, 2, 1408 // 2, 1, "zipf"), tile_n=tile_n)
+
+
+@pytest.mark.parametrize("d", [16, 80, 1040])
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_reduction_not_a_multiple_of_64(d, tile_m):
+    """d % 64 != 0: the last k-block holds d % 64 columns (1, 1 and 1 K=16 steps past
+    the 64-multiples for d = 16, 80, 1040); the MMAs stop at d in both tile shapes."""
+    plan, _ = _full_check(workloads.custom("dk", 600, d, 4, 2, 512, 2, "zipf"), tile_m=tile_m)
+    assert plan.info["tile_m"] == tile_m
 
 
 def test_all_rows_to_one_expert():
@@ -218,9 +228,10 @@ def test_pair_mode_last_tile_of_at_most_128_rows(T, tile_n):
     (1500, 4, 2, 1408),   # six column tiles, the last 128 wide
 ])
 def test_pair_mode_narrow_last_column_tile(T, E, k, N):
-    """256-wide pair tiles whose last column tile holds at most 128 columns (its B boxes
-    partly or wholly outside W).  Against the oracle, and (where 512-wide tiles exist,
-    N >= 512) bit for bit against 512-wide tiles: each element sees the same K order."""
+    """256-wide pair tiles whose last column tile holds at most 128 columns run it as an
+    N=128 pair MMA, one 64-column B box per CTA.  Against the oracle, and (where 512-wide
+    tiles exist, N >= 512) bit for bit against 512-wide tiles, which issue N=256 MMAs
+    only: each element sees the same K order."""
     wl = workloads.custom("narrow", T, 128, E, k, N, 1, "none")
     plan, bufs = _full_check(wl, tile_m=256, tile_n=256)
     assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
@@ -334,15 +345,7 @@ def test_bf16_output_mixtral_full_size_sampled():
     a_rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"][rows], wl.k)
     cols_t = torch.tensor(cols, device="cuda")
     got = bufs.Y[torch.tensor(rows, device="cuda")][:, cols_t].float().cpu().double().numpy()
-    want = np.empty_like(got)
-    cache = {}
-    for i, row in enumerate(rows):
-        e = oracle.expert_of_row(ref["offsets"], row)
-        if e not in cache:
-            cache[e] = workloads.bf16_bits(inp["W"][e][:, cols_t])
-        for j in range(len(cols)):
-            want[i, j] = oracle.gemm_entry(a_rows[i], cache[e], j)
-    _check_bf16(got, want)
+    _check_bf16(got, oracle_grid(a_rows, rows, inp["W"], ref, cols))
 
 
 def test_empty_batch_every_gemm_entry_point():

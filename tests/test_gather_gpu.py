@@ -43,6 +43,9 @@ def _both(wl, inp, **plan_kw):
     (1, 128, 8, 8, 128, 8, "none"),       # one token, k = E
     (500, 128, 1, 1, 256, 1, "none"),     # one expert: a plain GEMM with 4 row tiles
     (700, 256, 8, 2, 704, 1, "none"),
+    (300, 16, 4, 2, 256, 1, "none"),      # d = 16: one k-block of one K=16 step
+    (400, 80, 8, 2, 384, 2, "zipf"),      # d = 80: a last k-block of 16 columns
+    (257, 1040, 8, 2, 256, 1, "none"),    # d = 1040 = 16 * 65
 ])
 def test_gather_matches_dispatch_bitwise_and_oracle(T, d, E, k, N, R, bias):
     wl = workloads.custom("gat", T, d, E, k, N, R, bias)

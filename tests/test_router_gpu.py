@@ -45,6 +45,8 @@ def _bits(a):
     (10000, 128, 40, "zipf"),  # the second expert block holds 8 experts, the last token block 16 tokens
     (19457, 64, 32, "none"),   # the last CTA holds 1 token (its second-token rows all past T); one stage
     (4864, 192, 256, "hot4"),  # three stages, fewer than the ring's depth
+    # d % 64 != 0: the fallback kernel; d % 32 == 16 ends in a half chunk
+    (300, 16, 8, "none"), (257, 80, 24, "zipf"), (500, 1040, 64, "none"), (100, 48, 3, "none"),
 ])
 def test_router_logits_bit_exact(T, d, E, bias):
     wl = workloads.custom("router", T, d, E, 1, 16, 1, bias)

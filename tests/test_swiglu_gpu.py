@@ -18,7 +18,8 @@ import torch
 
 import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
-from tests.gpu_util import TOL_FRO, TOL_MAX_REL_RMS, check_recv, check_route, check_Y, sample_rows_cols
+from tests.gpu_util import (TOL_FRO, TOL_MAX_REL_RMS, check_recv, check_route, check_Y, oracle_grid,
+                            sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +72,8 @@ def _up_check(T, d, E, k, F, R, bias, seed=0, **plan_kw):
     (600, 128, 16, 4, 200, 4, "zipf", 0),    # skewed load, empty experts, tail of 72
     (500, 128, 4, 2, 136, 1, "none", 128),   # forced 128-wide tiles: 3 column tiles (64, 64, 8)
     (64, 256, 128, 8, 96, 1, "hot4", 0),     # decode-like
+    (300, 80, 4, 2, 144, 1, "none", 0),      # d = 80: a last k-block of 16 columns
+    (200, 1040, 4, 2, 128, 2, "none", 0),    # d = 1040
 ])
 def test_swiglu_up_full_parity(T, d, E, k, F, R, bias, tile_n):
     plan = _up_check(T, d, E, k, F, R, bias, tile_n=tile_n)
@@ -80,6 +83,7 @@ def test_swiglu_up_full_parity(T, d, E, k, F, R, bias, tile_n):
 @pytest.mark.parametrize("T,d,E,k,F", [
     (1000, 128, 2, 1, 272),   # 3 column tiles of 128 (128, 128, 16); odd halves at the tail
     (130, 64, 1, 1, 128),     # one expert, 130 rows: the odd half holds 2 rows
+    (600, 80, 2, 1, 272),     # d = 80: a last k-block of 16 columns
 ])
 def test_swiglu_up_pair_mode(T, d, E, k, F):
     plan = _up_check(T, d, E, k, F, 1, "none", tile_m=256)
@@ -141,6 +145,8 @@ def _grouped_check(T, d, E, k, N, bias, seed=0, **plan_kw):
     (700, 256, 8, 2, 512, "zipf"),
     (64, 256, 128, 8, 256, "hot4"),
     (1, 64, 8, 8, 128, "none"),
+    (300, 16, 4, 2, 272, "none"),    # K = 16
+    (500, 1040, 8, 2, 256, "zipf"),  # K = 1040
 ])
 def test_grouped_gemm_full_parity(T, d, E, k, N, bias):
     _grouped_check(T, d, E, k, N, bias)
@@ -149,8 +155,9 @@ def test_grouped_gemm_full_parity(T, d, E, k, N, bias):
 @pytest.mark.parametrize("T,E,N,tile_n", [(1000, 2, 400, 0), (1000, 2, 1040, 512),
                                           (1200, 4, 512, 0), (1200, 4, 512, 512),  # ~300-row experts: M=128 tails
                                           (1000, 2, 1408, 256)])  # a 128-wide last column tile
-def test_grouped_gemm_pair_mode(T, E, N, tile_n):
-    plan = _grouped_check(T, 128, E, 1, N, "none", tile_m=256, tile_n=tile_n)
+@pytest.mark.parametrize("d", [128, 80])
+def test_grouped_gemm_pair_mode(T, E, N, tile_n, d):
+    plan = _grouped_check(T, d, E, 1, N, "none", tile_m=256, tile_n=tile_n)
     assert plan.info["tile_m"] == 256 and (tile_n == 0 or plan.info["tile_n"] == tile_n)
 
 
@@ -237,16 +244,8 @@ def test_swiglu_mixtral_ffn_full_size_sampled():
     a_rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"][rows], k)
     got = bu.H[torch.tensor(rows, device="cuda")][:, torch.tensor(fcols, device="cuda")]
     got = got.float().cpu().double().numpy()
-    cols_gu = torch.tensor(list(fcols) + [F + f for f in fcols], device="cuda")
-    want = np.empty_like(got)
-    cache = {}
-    nf = len(fcols)
-    for i, row in enumerate(rows):
-        e = oracle.expert_of_row(ref["offsets"], row)
-        if e not in cache:
-            cache[e] = workloads.bf16_bits(W1[e][:, cols_gu])
-        G = np.array([[oracle.gemm_entry(a_rows[i], cache[e], j) for j in range(2 * nf)]])
-        want[i] = oracle.swiglu(G)[0]
+    G = oracle_grid(a_rows, rows, W1, ref, list(fcols) + [F + f for f in fcols])
+    want = oracle.swiglu(G)
     err = np.abs(got - want)
     rms = float(np.sqrt(np.mean(want ** 2)))
     assert (err <= H_REL * np.abs(want) + H_ABS * rms).all()
@@ -264,18 +263,11 @@ def test_swiglu_mixtral_ffn_full_size_sampled():
     rc, status = binding.moe_read_status(status_d)
     assert rc == 0, status
     assert not torch.isnan(Y2).any().item()
-    dcols = sorted({0, d - 1, 255, 256, d // 2} | set(np.random.default_rng(1).integers(0, d, 12).tolist()))
+    _, dcols = sample_rows_cols(ref, d, tile_n=256, seed=1)  # one column in every 64-column box
     dcols_t = torch.tensor(dcols, device="cuda")
     h_rows = workloads.bf16_bits(A[torch.tensor(rows, device="cuda")])
     got = Y2[torch.tensor(rows, device="cuda")][:, dcols_t].cpu().double().numpy()
-    want = np.empty_like(got)
-    cache = {}
-    for i, row in enumerate(rows):
-        e = oracle.expert_of_row(ref["offsets"], row)
-        if e not in cache:
-            cache[e] = workloads.bf16_bits(W2[e][:, dcols_t])
-        for j in range(len(dcols)):
-            want[i, j] = oracle.gemm_entry(h_rows[i], cache[e], j)
+    want = oracle_grid(h_rows, rows, W2, ref, dcols)
     err = np.abs(got - want)
     rms = float(np.sqrt(np.mean(want ** 2)))
     assert float(err.max()) <= TOL_MAX_REL_RMS * rms
