@@ -54,6 +54,13 @@ def _args(argv=None):
     ap.add_argument("--l2", choices=["flush", "none"], default="flush",
                     help="between timed steps: flush L2 (default) or rely on inputs larger than L2")
     ap.add_argument("--producer-ctas", type=int, default=0)
+    ap.add_argument("--workloads", default="others",
+                    help="other configurations measured in the same run: 'others' (every other "
+                         "workload), 'none', or a comma-separated list")
+    ap.add_argument("--kernel-only", choices=["fused", "grouped"], default=None,
+                    help="profiling case: after the warm-up, run only `--steps` launches of the fused "
+                         "kernel (moe_dispatch_gemm) or of the GEMM alone on the receive rows in place "
+                         "(moe_grouped_gemm), L2 flushed between them, print their median and exit")
     ap.add_argument("--ffn", choices=["auto", "on", "off"], default="auto",
                     help="also time the gated (SwiGLU) expert FFN with F = N (auto: Mixtral-shaped only)")
     return ap.parse_args(argv)
@@ -103,11 +110,76 @@ def _traffic_per_launch(workload: str):
         return None
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region.
+class NvmlClocks:
+    """Read-only NVML queries (libnvidia-ml through ctypes) of one GPU's SM clock and
+    clock-event reasons, polled by a thread of its own every PERIOD_S.  Nothing is set:
+    only nvmlInit, handle lookups, nvmlDeviceGet*Clock* and nvmlShutdown are called."""
 
-    The sampler starts before the region (nvidia-smi takes a moment to report) and
-    keeps only the samples whose own timestamps fall between entry and exit."""
+    PERIOD_S = 0.002
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int, uuid: str | None = None):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        self.rows = []
+        self._stop = threading.Event()
+        self._thread = None
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        ok = False
+        if uuid:
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            raise RuntimeError("no NVML handle")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0 \
+            else None
+        self.sample()  # one query now, so a failure shows before the timed region
+
+    def sample(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) != 0:  # NVML_CLOCK_SM
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        reasons = [n for b, n in self.REASON_BITS.items() if self._reasons(self.dev, ct.byref(rs)) == 0 and rs.value & b]
+        self.rows.append((time.time(), float(mhz.value), reasons))
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.sample()
+            except Exception:
+                return
+            time.sleep(self.PERIOD_S)
+
+    def start(self):
+        import threading
+        self.rows = []
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2.0)
+        self.sample()  # the clock at the region's end
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clocks and clock-event reasons during the timed region: NVML polled every
+    2 ms when libnvidia-ml can be loaded, else nvidia-smi every PERIOD_MS.
+
+    The nvidia-smi sampler starts before the region (nvidia-smi takes a moment to
+    report) and keeps only the samples whose own timestamps fall between entry and
+    exit."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -115,13 +187,29 @@ class ClockSampler:
     STARTUP_S = 0.5
     PERIOD_MS = 50
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, use_nvml: bool = True):
         self.index = index
         self.proc = None
         self.lines = []
         self.t0 = self.t1 = None
+        self.nvml = None
+        self.use_nvml = use_nvml
 
     def __enter__(self):
+        if self.use_nvml:
+            try:
+                uuid = None
+                try:
+                    import torch
+                    uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+                except Exception:
+                    pass
+                self.nvml = NvmlClocks(self.index, uuid)
+                self.t0 = time.time()
+                self.nvml.start()
+                return self
+            except Exception:
+                self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -136,6 +224,9 @@ class ClockSampler:
     def __exit__(self, *exc):
         self.t1 = time.time()
         self.lines = []
+        if self.nvml is not None:
+            self.nvml.stop()
+            return
         if self.proc is not None:
             time.sleep(2 * self.PERIOD_MS / 1000.0)  # the sample that covers the region's end
             self.proc.terminate()
@@ -154,6 +245,14 @@ class ClockSampler:
             return None
 
     def summary(self):
+        if self.nvml is not None:
+            inside = [r for r in self.nvml.rows if self.t0 <= r[0] <= self.t1 + 0.01]
+            if not inside:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
+            return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": self.nvml.max_mhz,
+                    "sm_mhz_min": min(r[1] for r in inside),
+                    "reasons": sorted({n for r in inside for n in r[2]}), "samples": len(inside),
+                    "window": "timed region", "period_ms": 1000 * NvmlClocks.PERIOD_S, "source": "nvml"}
         rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -198,6 +297,137 @@ def launches_per_step(wl) -> int:
     return 2 + (1 if wl.T * wl.k > 8192 else 0)
 
 
+LATENCY_BOUND_US = 10.0  # below this ideal time (HBM or tensor) a launch is latency-bound
+
+
+def roofline_of(wl, touched: int, fused_avg_s: float, plan_info: dict, peaks) -> dict:
+    """Roofline of the fused kernel from its algorithmic work (algorithmic_work) and its
+    average launch time: "tensor" when the FLOP per byte exceed the measured ridge,
+    "hbm" otherwise, "latency" when both ideal times are below LATENCY_BOUND_US."""
+    hbm_peak, tf_peak, tf_sustained, peak_src = peaks
+    flops, alg_bytes, _ = algorithmic_work(wl, touched)
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
+    t_tensor_us = flops / (tf_peak * 1e12) * 1e6
+    t_hbm_us = alg_bytes / (hbm_peak * 1e9) * 1e6
+    if flops / alg_bytes >= ridge:
+        roof = {"bound": "tensor", "achieved": flops / fused_avg_s / 1e12, "peak": tf_peak,
+                "unit": "TFLOP/s", "peak_source": f"{peak_src} (bf16 burst)"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg_bytes / fused_avg_s / 1e9, "peak": hbm_peak,
+                "unit": "GB/s", "peak_source": f"{peak_src} (copy bandwidth)"}
+    if max(t_tensor_us, t_hbm_us) < LATENCY_BOUND_US:
+        roof["bound"] = "latency"
+        roof["note"] = (f"ideal times {t_hbm_us:.2f} us (HBM) and {t_tensor_us:.2f} us (tensor) are far "
+                        f"below the launch and pipeline latency; achieved/frac against "
+                        f"{'HBM' if roof['unit'] == 'GB/s' else 'bf16'} for reference")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    if roof["bound"] == "tensor":  # the same kernel against the power-capped sustained peak
+        roof["peak_sustained"] = tf_sustained
+        roof["frac_sustained"] = roof["achieved"] / tf_sustained
+    roof["traffic"] = _traffic_per_launch(wl.name)
+    tile = f"{plan_info['tile_m']}x{plan_info['tile_n']} tiles"
+    roof["kernel"] = (f"dispatch_gemm_pair_kernel (CTA pairs, {tile})"
+                      if plan_info["tile_m"] == 256 else f"dispatch_gemm_kernel ({tile})")
+    roof["algorithmic_flops"] = flops
+    roof["algorithmic_bytes"] = alg_bytes
+    return roof
+
+
+def trace_summary(tr, num_ctas: int, fields) -> dict:
+    """Per-CTA trace records of one launch (rows of kTraceWords int64) -> [median, max]
+    over CTAs of each phase stamp, in us from the first CTA's start."""
+    tr = tr.view(-1, len(fields))[:num_ctas].cpu().double()
+    fi = {n: i for i, n in enumerate(fields)}
+    t0 = tr[:, fi["start"]].min()
+    us = lambda col, rows=slice(None): ((tr[rows, fi[col]] - t0) / 1e3)
+    loaded = tr[:, fi["tiles"]] > 0  # CTAs that loaded at least one tile
+    scattered = tr[:, fi["scatter_end"]] > 0
+    med_max = lambda v: [float(v.median()), float(v.max())] if v.numel() else None
+    return {
+        "scatter_end_us": med_max(us("scatter_end", scattered)),
+        "first_tile_us": med_max(us("first_tile", loaded)),
+        "flag_wait_us": med_max(tr[loaded, fi["flag_wait_ns"]] / 1e3),
+        "end_us": med_max(us("end")),
+        "ctas_with_tiles": int(loaded.sum()),
+        "note": "one traced launch of the fused kernel, per-CTA global-timer stamps from the first CTA's "
+                "start: [median, max] over CTAs",
+    }
+
+
+def measure_workload(wl, K: int, warmup: int, dev, stream, flush, l2: str = "flush") -> dict:
+    """The whole path (route + fused dispatch/grouped GEMM) of one workload in the plan's
+    own launch configuration: K timed steps (CUDA events on the launching stream, L2
+    flushed between steps), nvidia-smi clocks during the timed region, the roofline of
+    the fused kernel, the scatter window and one traced launch.  Used for every
+    configuration besides the headline one."""
+    import torch
+
+    from moe_token_dispatch_route_gb300 import binding, workloads
+
+    inp = workloads.make_inputs(wl, seed=0, w_device=dev)
+    x, W, logits = inp["x"].to(dev), inp["W"], inp["logits"].to(dev)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, device=dev.index)
+    bufs = binding.MoeBuffers(plan, dev)
+    for _ in range(max(3, warmup)):
+        binding.forward(plan, logits, x, W, bufs, stream)
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"{wl.name}: device status after warm-up: {st}")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for i in range(K):
+            if l2 == "flush":
+                flush.fill_(float(i))
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            binding.route(plan, logits, bufs, stream)
+            e1.record(stream)
+            binding.dispatch_gemm(plan, x, W, bufs, stream)
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"{wl.name}: device status after timed steps: {st}")
+    hdr = bufs.workspace[:64].cpu().numpy().view("uint64")
+    scatter_ns = int(hdr[25]) - int(hdr[24])
+    touched = int((bufs.counts > 0).sum().item())
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dg_ms = [b.elapsed_time(c) for _, b, c in ev]
+    trace = torch.zeros(plan.info["sm_count"] * binding.TRACE_WORDS, dtype=torch.int64, device=dev)
+    binding.moe_set_trace(plan, trace)
+    flush.fill_(2.0)
+    binding.dispatch_gemm(plan, x, W, bufs, stream)
+    torch.cuda.synchronize(dev)
+    binding.moe_set_trace(plan, None)
+    tr = trace_summary(trace, plan.info["num_ctas"], binding.TRACE_FIELDS)
+    _, _, scatter_bytes = algorithmic_work(wl, touched)
+    peaks = _peaks()
+    roof = roofline_of(wl, touched, statistics.mean(dg_ms) / 1000.0, plan.info, peaks)
+    out = {
+        "config": {**wl.describe(), "tile_m": plan.info["tile_m"], "tile_n": plan.info["tile_n"],
+                   "num_ctas": plan.info["num_ctas"], "producer_ctas": plan.info["producer_ctas"]},
+        "steps": K,
+        "step_ms": statistics.median(step_ms),
+        "route_ms": statistics.median([a.elapsed_time(b) for a, b, _ in ev]),
+        "fused_ms": statistics.median(dg_ms),
+        "fused_mean_ms": statistics.mean(dg_ms),
+        "tflops": wl.flops / (statistics.median(step_ms) * 1e9),
+        "tokens_per_s": wl.T / (statistics.median(step_ms) / 1000.0),
+        "roofline": roof,
+        "scatter": {"window_ms": scatter_ns / 1e6, "bytes": scatter_bytes,
+                    "gbs": scatter_bytes / max(scatter_ns, 1),
+                    "frac_hbm": scatter_bytes / max(scatter_ns, 1) / peaks[0]},
+        "touched_experts": touched,
+        "trace": tr,
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step(wl) * K,
+    }
+    del bufs, W, x, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -216,12 +446,23 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+MULTICORE_WORKLOADS = ("mixtral", "finegrained", "deepseek_v3")  # oracle split over all host cores
+
+
+def oracle_threads(wl) -> int:
+    """Host threads of the oracle's timed GEMM: all cores on the Mixtral-, fine-grained-
+    and DeepSeek-V3-shaped layers, one on the tiny and decode layers."""
+    return max(1, os.cpu_count() or 1) if wl.name in MULTICORE_WORKLOADS else 1
+
+
 class OracleSample:
     """The CPU oracle, as it stands, on a bounded sample of one workload.
 
     One sample = routing of all T tokens (top-k, histogram, permutation), then
-    gather + fp64 grouped GEMM of the first `rows` destination rows.  Inputs and
-    the weight slice those rows need are prepared once, outside any timing."""
+    gather + fp64 grouped GEMM of the first `rows` destination rows, the GEMM's
+    output rows split over `threads` host threads (each the single-threaded oracle
+    on its own rows; the result is bitwise the single-threaded one).  Inputs and the
+    weight slice those rows need are prepared once, outside any timing."""
 
     def __init__(self, wl, max_rows=512):
         import numpy as np
@@ -236,13 +477,12 @@ class OracleSample:
         self.xb = workloads.bf16_bits(inp["x"])
         ref = oracle.route(self.L, wl.k)
         rows = min(max_rows, wl.S)
-        experts = sorted({oracle.expert_of_row(ref["offsets"], r) for r in range(rows)})
-        self.n_exp = max(experts) + 1
+        self.n_exp = oracle.expert_of_row(ref["offsets"], rows - 1) + 1
         W = workloads.make_weights(workloads.custom("w", wl.T, wl.d, self.n_exp, 1, wl.N), seed=0)
         self.Wb = workloads.bf16_bits(W)
         self.np = np
 
-    def run(self, rows):
+    def run(self, rows, threads=1):
         """Time one sample; returns (seconds, GEMM FLOPs of the sample)."""
         o, np = self.oracle, self.np
         rows = min(rows, self.wl.S)
@@ -250,22 +490,37 @@ class OracleSample:
         ref = o.route(self.L, self.wl.k)
         a_rows = o.gather(self.xb, ref["perm"][:rows], self.wl.k)
         off = np.minimum(ref["offsets"][: self.n_exp + 1], rows).astype(np.int32)
-        o.grouped_gemm(a_rows, self.Wb[: self.n_exp], off)
+        if threads > 1:
+            o.grouped_gemm_parallel(a_rows, self.Wb[: self.n_exp], off, threads)
+        else:
+            o.grouped_gemm(a_rows, self.Wb[: self.n_exp], off)
         secs = time.perf_counter() - t0
         return secs, 2.0 * rows * self.wl.d * self.wl.N
 
-    def describe(self, rows, secs):
+    def describe(self, rows, secs, threads=1):
         return {"sample": f"routing of all {self.wl.T} tokens + gather and fp64 GEMM of the first "
-                          f"{rows} destination rows, {secs:.2f} s; TFLOP/s = sampled GEMM FLOPs / "
-                          f"sample time", "cores": 1, "kind": "oracle"}
+                          f"{rows} destination rows (output rows split over {threads} host threads), "
+                          f"{secs:.2f} s; TFLOP/s = sampled GEMM FLOPs / sample time",
+                "cores": threads, "kind": "oracle"}
 
 
-def cpu_baseline(wl, rows=384):
-    """The oracle timed once on about 10-20 s of single-core work (384 rows on the
-    Mixtral-shaped layer); returns (TFLOP/s, info)."""
+def _oracle_rows(wl, threads: int, seconds: float) -> int:
+    """Destination rows of an oracle sample that takes about `seconds` on `threads`
+    host threads, from a timed 8-row single-thread calibration."""
+    cal = OracleSample(wl, max_rows=8)
+    secs8, _ = cal.run(8)
+    per_row = max(secs8, 1e-4) / 8
+    return max(1, min(wl.S, int(threads * seconds / per_row)))
+
+
+def cpu_baseline(wl, seconds=15.0):
+    """The oracle timed once on about `seconds` of work on the host cores (all of
+    them on the three large layers); returns (TFLOP/s, info, seconds)."""
+    threads = oracle_threads(wl)
+    rows = _oracle_rows(wl, threads, seconds)
     s = OracleSample(wl, max_rows=rows)
-    secs, flops = s.run(rows)
-    return flops / secs / 1e12, s.describe(rows, secs), secs
+    secs, flops = s.run(rows, threads)
+    return flops / secs / 1e12, s.describe(rows, secs, threads), secs
 
 
 def run_reference(args, wl):
@@ -273,20 +528,20 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     # each step is one oracle sample, sized so that warm-up + timed steps take about two minutes
-    sample = OracleSample(wl)
-    secs8, _ = sample.run(8)
+    threads = oracle_threads(wl)
     per_step = max(0.2, 120.0 / max(1, args.steps + args.warmup))
-    rows = max(1, min(512, int(8 * per_step / max(secs8, 1e-4))))
+    rows = _oracle_rows(wl, threads, per_step)
+    sample = OracleSample(wl, max_rows=rows)
     for _ in range(args.warmup):
-        sample.run(rows)
+        sample.run(rows, threads)
     times = []
     flops = 0.0
     for _ in range(args.steps):
-        secs, flops = sample.run(rows)
+        secs, flops = sample.run(rows, threads)
         times.append(secs)
     total = sum(times)
     value = len(times) * flops / total / 1e12
-    info = sample.describe(rows, statistics.median(times))
+    info = sample.describe(rows, statistics.median(times), threads)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -356,6 +611,52 @@ def time_swiglu_ffn(wl, inp, x, logits, dev, stream, flush, reps=20):
     res["tile_m"] = [up.info["tile_m"], down.info["tile_m"]]
     del W1, W2, bu, Y2, out
     return res
+
+
+def run_kernel_only(args, wl):
+    """A short run for profilers: route once, warm up, then `args.steps` launches of one
+    kernel with L2 flushed between them; prints one JSON line with their median."""
+    import torch
+
+    from moe_token_dispatch_route_gb300 import binding, build as _build, workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    inp = workloads.make_inputs(wl, seed=0, w_device=dev)
+    x, W, logits = inp["x"].to(dev), inp["W"], inp["logits"].to(dev)
+    plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_n=args.tile_n,
+                            tile_m=args.tile_m, producer_ctas=args.producer_ctas, device=0)
+    bufs = binding.MoeBuffers(plan, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    binding.forward(plan, logits, x, W, bufs, stream)  # routing + receive rows in place
+    ws = torch.zeros(plan.workspace_bytes // 4 + 64, dtype=torch.int32, device=dev)
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    if args.kernel_only == "fused":
+        launch = lambda: binding.dispatch_gemm(plan, x, W, bufs, stream)
+    else:
+        if wl.R != 1:
+            raise SystemExit("--kernel-only grouped needs one rank buffer (R = 1)")
+        launch = lambda: binding.moe_grouped_gemm(plan, bufs.recv[0], bufs.offsets, W, bufs.Y, ws, st, stream)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        launch()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in evs:
+        flush.fill_(1.0)
+        a_.record(stream)
+        launch()
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    for s_ in (bufs.status, st):
+        rc, words = binding.moe_read_status(s_, stream)
+        if rc != 0:
+            raise SystemExit(f"device status: {words}")
+    print(json.dumps({"kernel_only": args.kernel_only, "config": wl.describe(), "launches": args.steps,
+                      "ms": statistics.median(a_.elapsed_time(b_) for a_, b_ in evs),
+                      "tile_m": plan.info["tile_m"], "tile_n": plan.info["tile_n"]}), flush=True)
+    return 0
 
 
 def run_ours(args, wl):
@@ -458,22 +759,7 @@ def run_ours(args, wl):
     binding.dispatch_gemm(plan, x, W, bufs, stream)
     torch.cuda.synchronize(dev)
     binding.moe_set_trace(plan, None)
-    tr = trace.view(-1, binding.TRACE_WORDS)[: plan.info["num_ctas"]].cpu().double()
-    fi = {n: i for i, n in enumerate(binding.TRACE_FIELDS)}
-    t0 = tr[:, fi["start"]].min()
-    us = lambda col, rows=slice(None): ((tr[rows, fi[col]] - t0) / 1e3)
-    loaded = tr[:, fi["tiles"]] > 0  # CTAs that loaded at least one tile
-    scattered = tr[:, fi["scatter_end"]] > 0
-    med_max = lambda v: [float(v.median()), float(v.max())] if v.numel() else None
-    trace_info = {
-        "scatter_end_us": med_max(us("scatter_end", scattered)),
-        "first_tile_us": med_max(us("first_tile", loaded)),
-        "flag_wait_us": med_max(tr[loaded, fi["flag_wait_ns"]] / 1e3),
-        "end_us": med_max(us("end")),
-        "ctas_with_tiles": int(loaded.sum()),
-        "note": "one traced launch of the fused kernel, per-CTA global-timer stamps from the first CTA's "
-                "start: [median, max] over CTAs",
-    }
+    trace_info = trace_summary(trace, plan.info["num_ctas"], binding.TRACE_FIELDS)
     del trace
 
     # the same step captured once in a CUDA graph and replayed (launch overhead removed)
@@ -536,6 +822,34 @@ def run_ours(args, wl):
         raise SystemExit(f"device status after the bf16-output timing: {st}")
     ybf16_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in bev)
     del bufs_b, plan_b
+
+    # the combine fused into the GEMM epilogue (k <= 2): a memset of the output and one
+    # launch, against the unfused chain (the fused kernel writing Y + moe_combine reading it)
+    fused_combine = None
+    if wl.k <= 2:
+        comb_out = torch.empty(wl.T, wl.N, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            binding.dispatch_gemm_combine(plan, x, W, bufs, comb_out, stream)
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        for a_, b_ in fev:
+            flush.fill_(1.0)
+            a_.record(stream)
+            binding.dispatch_gemm_combine(plan, x, W, bufs, comb_out, stream)
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        rc, st = binding.moe_read_status(bufs.status, stream)
+        if rc != 0:
+            raise SystemExit(f"device status after the fused-combine timing: {st}")
+        fc_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in fev)
+        unfused = statistics.median(dg_ms) + combine_ms
+        fused_combine = {"ms": fc_ms, "unfused_ms": unfused, "speedup_vs_unfused": unfused / fc_ms,
+                         "tflops": wl.flops / (fc_ms * 1e9),
+                         "note": "moe_dispatch_gemm_combine: zero-fill of out [T, N] + the fused kernel "
+                                 "whose epilogue adds each gate-weighted row into its token's row "
+                                 "(fp32 reductions, reproducible for k <= 2); unfused = fused kernel "
+                                 "(writes Y) + moe_combine; 20 launches, L2 flushed; not in value"}
+        del comb_out
+        binding.dispatch_gemm(plan, x, W, bufs, stream)  # leave Y as the path computes it
 
     ffn = None
     if args.ffn == "on" or (args.ffn == "auto" and wl.name == "mixtral"):
@@ -601,27 +915,26 @@ def run_ours(args, wl):
     if rank != 0:
         return 0
 
+    # every other configuration of the benchmark, each in its own plan's launch
+    # configuration, measured in the same run (rank 0 only)
+    others = {}
+    names = [] if args.workloads == "none" else (
+        [n for n in workloads.WORKLOADS if n != wl.name] if args.workloads == "others"
+        else [n for n in args.workloads.split(",") if n and n != wl.name])
+    if names:
+        del sets, bufs, W, x, logits, inp, flush
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        for name in names:
+            others[name] = measure_workload(workloads.WORKLOADS[name], max(20, K), args.warmup, dev,
+                                            stream, flush, args.l2)
+
     hbm_peak, tf_peak, tf_sustained, peak_src = _peaks()
     flops, alg_bytes, scatter_bytes = algorithmic_work(wl, touched)
     value = world * K * flops / total_s / 1e12
     dg_avg_s = statistics.mean(dg_ms) / 1000.0
-    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
-    if flops / alg_bytes >= ridge:
-        roof = {"bound": "tensor", "achieved": flops / dg_avg_s / 1e12, "peak": tf_peak,
-                "unit": "TFLOP/s", "peak_source": f"{peak_src} (bf16 burst)"}
-    else:
-        roof = {"bound": "hbm", "achieved": alg_bytes / dg_avg_s / 1e9, "peak": hbm_peak,
-                "unit": "GB/s", "peak_source": f"{peak_src} (copy bandwidth)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    if roof["bound"] == "tensor":  # the same kernel against the power-capped sustained peak
-        roof["peak_sustained"] = tf_sustained
-        roof["frac_sustained"] = roof["achieved"] / tf_sustained
-    roof["traffic"] = _traffic_per_launch(wl.name)
-    tile = f"{plan.info['tile_m']}x{plan.info['tile_n']} tiles"
-    roof["kernel"] = (f"dispatch_gemm_pair_kernel (CTA pairs, {tile})"
-                      if plan.info["tile_m"] == 256 else f"dispatch_gemm_kernel ({tile})")
-    roof["algorithmic_flops"] = flops
-    roof["algorithmic_bytes"] = alg_bytes
+    roof = roofline_of(wl, touched, dg_avg_s, plan.info, (hbm_peak, tf_peak, tf_sustained, peak_src))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / K, "higher_is_better": True,
@@ -664,6 +977,7 @@ def run_ours(args, wl):
         "y_bf16": {"ms": ybf16_ms, "tflops": flops / (ybf16_ms * 1e9),
                    "note": "moe_dispatch_gemm with out_dtype = MOE_OUT_BF16 (Y rounded once to bf16, "
                            "half the Y bytes); 20 launches, L2 flushed; not in value"},
+        "combine_fused": fused_combine,
         "swiglu_ffn": ffn,
         "e2e": {"value": world * E2E * flops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2E,
@@ -673,6 +987,7 @@ def run_ours(args, wl):
                            f"no flush: the weights ({w_bytes >> 20} MiB) exceed the L2")},
         "gpu_launches": launches_per_step(wl) * K,
         "clocks": clk.summary(),
+        "workloads": others or None,
     }
     if not args.no_cpu_baseline:
         v, info, _ = cpu_baseline(wl)
@@ -691,6 +1006,8 @@ def main(argv=None):
         wl = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.kernel_only:
+        return run_kernel_only(args, wl)
     return run_ours(args, wl)
 
 

@@ -101,3 +101,18 @@ def test_max_over_ranks_gloo_two_processes():
 
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_clock_summary_from_nvml_samples():
+    """NVML samples (time, SM MHz, reasons): only those inside the timed region count."""
+    import types
+    c = bench.ClockSampler(0)
+    c.t0 = time.time()
+    c.t1 = c.t0 + 0.02
+    c.nvml = types.SimpleNamespace(max_mhz=2070.0, rows=[
+        (c.t0 - 0.5, 900.0, []),                       # before the region
+        (c.t0 + 0.002, 2070.0, []), (c.t0 + 0.004, 1980.0, ["sw_power_cap"]),
+        (c.t0 + 0.006, 2010.0, []), (c.t0 + 5.0, 700.0, ["hw_slowdown"])])  # after it
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2010.0 and s["sm_mhz_min"] == 1980.0
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070.0 and s["source"] == "nvml"
