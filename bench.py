@@ -401,6 +401,27 @@ def measure_workload(wl, K: int, warmup: int, dev, stream, flush, l2: str = "flu
     torch.cuda.synchronize(dev)
     binding.moe_set_trace(plan, None)
     tr = trace_summary(trace, plan.info["num_ctas"], binding.TRACE_FIELDS)
+
+    def median_ms(fn, n=10):
+        for _ in range(2):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a_, b_ in evs:
+            flush.fill_(1.0)
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    # the step after the path: moe_combine on Y, and the combine fused into the epilogue
+    comb_out = torch.empty(wl.T, wl.N, dtype=torch.float32, device=dev)
+    combine_ms = median_ms(lambda: binding.moe_combine(plan, bufs.Y, bufs.topk_w, bufs.dest, comb_out, stream))
+    fused_comb_ms = median_ms(lambda: binding.dispatch_gemm_combine(plan, x, W, bufs, comb_out, stream))
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"{wl.name}: device status after the combine timing: {st}")
+    del comb_out
     _, _, scatter_bytes = algorithmic_work(wl, touched)
     peaks = _peaks()
     roof = roofline_of(wl, touched, statistics.mean(dg_ms) / 1000.0, plan.info, peaks)
@@ -420,6 +441,10 @@ def measure_workload(wl, K: int, warmup: int, dev, stream, flush, l2: str = "flu
                     "frac_hbm": scatter_bytes / max(scatter_ns, 1) / peaks[0]},
         "touched_experts": touched,
         "trace": tr,
+        "combine": {"unfused_ms": statistics.median(dg_ms) + combine_ms, "combine_ms": combine_ms,
+                    "fused_ms": fused_comb_ms,
+                    "note": "fused kernel + moe_combine against moe_dispatch_gemm_combine; 10 launches "
+                            "each, L2 flushed; not in step_ms"},
         "clocks": clk.summary(),
         "gpu_launches": launches_per_step(wl) * K,
     }
@@ -823,10 +848,10 @@ def run_ours(args, wl):
     ybf16_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in bev)
     del bufs_b, plan_b
 
-    # the combine fused into the GEMM epilogue (k <= 2): a memset of the output and one
-    # launch, against the unfused chain (the fused kernel writing Y + moe_combine reading it)
+    # the combine fused into the GEMM epilogue: one launch, against the unfused chain (the
+    # fused kernel writing Y + moe_combine reading it)
     fused_combine = None
-    if wl.k <= 2:
+    if True:
         comb_out = torch.empty(wl.T, wl.N, dtype=torch.float32, device=dev)
         for _ in range(3):
             binding.dispatch_gemm_combine(plan, x, W, bufs, comb_out, stream)
@@ -844,10 +869,10 @@ def run_ours(args, wl):
         unfused = statistics.median(dg_ms) + combine_ms
         fused_combine = {"ms": fc_ms, "unfused_ms": unfused, "speedup_vs_unfused": unfused / fc_ms,
                          "tflops": wl.flops / (fc_ms * 1e9),
-                         "note": "moe_dispatch_gemm_combine: zero-fill of out [T, N] + the fused kernel "
-                                 "whose epilogue adds each gate-weighted row into its token's row "
-                                 "(fp32 reductions, reproducible for k <= 2); unfused = fused kernel "
-                                 "(writes Y) + moe_combine; 20 launches, L2 flushed; not in value"}
+                         "note": "moe_dispatch_gemm_combine: the fused kernel whose epilogue writes each "
+                                 "gate-weighted row into its token's row of out [T, N] (stored by the "
+                                 "token's lowest expert, then added in expert order), no Y; unfused = "
+                                 "fused kernel (writes Y) + moe_combine; 20 launches, L2 flushed; not in value"}
         del comb_out
         binding.dispatch_gemm(plan, x, W, bufs, stream)  # leave Y as the path computes it
 
@@ -972,7 +997,8 @@ def run_ours(args, wl):
                           "dispatch_gemm_ms": statistics.median(dg_ms),
                           "speedup_vs_dispatch": statistics.median(dg_ms) / gather_ms,
                           "note": "moe_gather_gemm: A rows copied from x by perm straight into the "
-                                  "GEMM's shared memory, no receive buffers (single-CTA kernel); "
+                                  "GEMM's shared memory by cp.async warps, no receive buffers (256-wide single-CTA tiles "
+                                  "on an automatic pair plan); "
                                   "20 launches, L2 flushed; not in value"},
         "y_bf16": {"ms": ybf16_ms, "tflops": flops / (ybf16_ms * 1e9),
                    "note": "moe_dispatch_gemm with out_dtype = MOE_OUT_BF16 (Y rounded once to bf16, "

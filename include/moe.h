@@ -227,28 +227,31 @@ MOE_API moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x,
  * moe_dispatch_gemm_combine -- moe_dispatch_gemm with the combine step (the
  * reverse exchange that the "MoE Dispatch + GEMM" row of the articles' table
  * of fused kernels implies after the per-expert GEMM) fused into the GEMM's
- * epilogue: instead of writing Y, each destination row i, times the gate of
- * its slot s = perm[i], is added into its token's output row:
+ * epilogue: no Y is written; each destination row i, times the gate of its
+ * slot s = perm[i], goes straight into its token's output row:
  *   out[t][n] = sum_{j<k} topk_w[t][j] * (x[t] . W[topk_idx[t][j]][:, n]),
- * each product rounded to fp32 and added with fp32 reductions in global
- * memory (no Y round trip, no separate combine launch).  For k <= 2 the
- * result does not depend on the order in which the two reductions land (a
- * two-term fp32 sum into a zeroed row is commutative), so it is the same on
- * every run, role split and grid size; it differs from moe_combine's
- * fused multiply-adds by at most the rounding of one product.
+ * with each product rounded to fp32 and the terms summed in fp32 in
+ * ascending expert order.  The token's lowest expert stores its term; each
+ * higher expert's term is added (a 16-byte fp32 reduction) only after the
+ * lower terms of that token and column tile have landed: every 128-row tile
+ * publishes an epoch-tagged completion word per column tile, and a row waits
+ * for the words of its token's lower rows.  Those tiles belong to lower
+ * experts, which the schedule claims first, so the waits always end; the
+ * order of the additions, and so every bit of `out`, does not depend on
+ * timing, role split or grid size, for any k.  It differs from moe_combine's
+ * fused multiply-adds by the rounding of each product.  Nothing is zeroed:
+ * every element of `out` is written by its token's first term.
+ *   dest   in:  int32 [T*k] from moe_route (device).
  *   topk_w in:  fp32 [T][k] from moe_route (device).
- *   out    out: fp32 [T][N], 16-byte aligned.  The call zeroes it
- *               (cudaMemsetAsync on `stream`) before its launch.
+ *   out    out: fp32 [T][N], 16-byte aligned.
  * Other arguments as for moe_dispatch_gemm (the receive buffers are written;
- * no Y is written whatever the plan's out_dtype).  MOE_ERR_UNSUPPORTED for
- * k > 2, where the reductions' order would change the bits: use
- * moe_dispatch_gemm + moe_combine there.  Launches a memset and one kernel.
+ * the plan's out_dtype does not apply).  Launches one kernel.
  */
 MOE_API moe_status_t moe_dispatch_gemm_combine(moe_plan_t plan, const uint16_t* x,
                                        const int32_t* offsets, const int32_t* perm,
-                                       const float* topk_w, const uint16_t* W,
-                                       void* const* recv, float* out, void* workspace,
-                                       int32_t* dev_status, void* stream);
+                                       const int32_t* dest, const float* topk_w,
+                                       const uint16_t* W, void* const* recv, float* out,
+                                       void* workspace, int32_t* dev_status, void* stream);
 
 /*
  * moe_dispatch_gemm_swiglu -- moe_dispatch_gemm for a gated (SwiGLU) expert
@@ -275,12 +278,15 @@ MOE_API moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x
 /*
  * moe_gather_gemm -- the per-expert grouped GEMM with its A rows gathered
  * straight from the token rows: for each destination row i, row x[perm[i] / k]
- * is copied from global memory into the GEMM's shared-memory tile, with no
- * receive buffer in between (a variant of moe_dispatch_gemm for one GPU, where
- * the all-to-all has no wire to cross; it measures what landing the rows in a
- * receive buffer costs).  Y is bit for bit the Y of moe_dispatch_gemm on a
- * plan with the same tile shape.  CTA-pair plans run it in the single-CTA
- * kernel with 256-wide tiles.
+ * is copied from global memory into the GEMM's shared-memory tile by 16-byte
+ * asynchronous copies of two warps per CTA, with no receive buffer in between (a
+ * variant of moe_dispatch_gemm for one GPU, where the all-to-all has no wire
+ * to cross; it measures what landing the rows in a receive buffer costs).  Y is
+ * bit for bit the Y of moe_dispatch_gemm with the same tile shape.  A plan made
+ * with tile_m = 256 runs it on CTA pairs (the peer's gathered stages are passed
+ * to the leader by a relay thread); an automatic plan that chose CTA pairs runs
+ * it in the single-CTA kernel with 256-wide tiles, where it is about twice as
+ * fast.
  *   x, offsets, perm, W, Y, workspace, dev_status, stream: as for
  *   moe_dispatch_gemm.  No receive buffers.  Launches one kernel.
  */

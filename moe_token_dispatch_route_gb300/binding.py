@@ -93,7 +93,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_route_biased.restype = I32
     lib.moe_dispatch_gemm.argtypes = [VP] * 10
     lib.moe_dispatch_gemm.restype = I32
-    lib.moe_dispatch_gemm_combine.argtypes = [VP] * 11
+    lib.moe_dispatch_gemm_combine.argtypes = [VP] * 12
     lib.moe_dispatch_gemm_combine.restype = I32
     lib.moe_dispatch_gemm_swiglu.argtypes = [VP] * 10
     lib.moe_dispatch_gemm_swiglu.restype = I32
@@ -210,11 +210,12 @@ def moe_dispatch_gemm(plan: Plan, x, offsets, perm, W, recv: Sequence, Y, worksp
     _check(rc, "moe_dispatch_gemm")
 
 
-def moe_dispatch_gemm_combine(plan: Plan, x, offsets, perm, topk_w, W, recv: Sequence, out, workspace,
+def moe_dispatch_gemm_combine(plan: Plan, x, offsets, perm, dest, topk_w, W, recv: Sequence, out, workspace,
                               dev_status, stream=None) -> None:
-    """Fused dispatch + grouped GEMM + combine (k <= 2): out[t] = sum_j w[t,j] * (x[t] W[e_j])."""
+    """Fused dispatch + grouped GEMM + combine: out[t] = sum_j w[t,j] * (x[t] W[e_j]), summed in
+    ascending expert order (no Y)."""
     arr = (ctypes.c_void_p * max(1, len(recv)))(*[_ptr(r) for r in recv])
-    rc = load_library().moe_dispatch_gemm_combine(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm),
+    rc = load_library().moe_dispatch_gemm_combine(plan.handle, _ptr(x), _ptr(offsets), _ptr(perm), _ptr(dest),
                                                   _ptr(topk_w), _ptr(W), ctypes.cast(arr, ctypes.c_void_p),
                                                   _ptr(out), _ptr(workspace), _ptr(dev_status),
                                                   _stream(stream, plan.device))
@@ -222,7 +223,7 @@ def moe_dispatch_gemm_combine(plan: Plan, x, offsets, perm, topk_w, W, recv: Seq
 
 
 def dispatch_gemm_combine(plan: Plan, x, W, bufs: "MoeBuffers", out, stream=None):
-    moe_dispatch_gemm_combine(plan, x, bufs.offsets, bufs.perm, bufs.topk_w, W, bufs.recv, out,
+    moe_dispatch_gemm_combine(plan, x, bufs.offsets, bufs.perm, bufs.dest, bufs.topk_w, W, bufs.recv, out,
                               bufs.workspace, bufs.status, stream)
 
 

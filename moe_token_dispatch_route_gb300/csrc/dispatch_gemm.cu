@@ -78,6 +78,7 @@ struct PieceRec {
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
+    uint64_t afull[kMaxStages];  // gather mode, peer CTA of a pair: its gather warps' rows landed
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t sfull[kRing];
@@ -491,13 +492,19 @@ __device__ __forceinline__ void store_block_rows(float* tile, const uint32_t (&v
 }
 
 // Combine epilogue: the same transposed block, each row scaled by its slot's gate and
-// added into its token's row of `out` with 16-byte fp32 reductions (red.global.add).
-// `col0`: Y column of the block's column 0; `tok_lane` / `w_lane`: token and gate of
-// the block's row `lane`.  With at most two slots per token the two reductions into a
-// zeroed row give fl(a + b) in either order, so the result does not depend on timing.
+// written into its token's row of `out`: stored by the token's first contribution (its
+// lowest expert), added with a 16-byte fp32 reduction (red.global.add) by the others,
+// which run only once the lower contributions have landed (combine_wait_lower).  `col0`:
+// Y column of the block's column 0; `c`: the combine row of the block's row `lane`.
+struct CombineRow {
+    int tok;    // token of the row (0 past the tile's rows)
+    float w;    // gate of the row's slot
+    int first;  // 1: the token's lowest expert (store), 0: a later one (add)
+};
+
 __device__ __forceinline__ void red_block_rows(float* tile, const uint32_t (&v)[32], float* out, size_t ld,
                                                int col0, int rows_valid, int cols_valid, int lane,
-                                               int tok_lane, float w_lane) {
+                                               const CombineRow& c) {
     float4* mine = reinterpret_cast<float4*>(tile + lane * kEpiStride);
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -509,31 +516,93 @@ __device__ __forceinline__ void red_block_rows(float* tile, const uint32_t (&v)[
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int row = 4 * j + sub;
-        const int t = __shfl_sync(kFull, tok_lane, row);
-        const float w = __shfl_sync(kFull, w_lane, row);
+        const int t = __shfl_sync(kFull, c.tok, row);
+        const float w = __shfl_sync(kFull, c.w, row);
+        const int first = __shfl_sync(kFull, c.first, row);
         if (row < rows_valid && col < cols_valid) {
             float4 y = *reinterpret_cast<const float4*>(tile + row * kEpiStride + col);
             y.x *= w;
             y.y *= w;
             y.z *= w;
             y.w *= w;
-            atomicAdd(reinterpret_cast<float4*>(out + (size_t)t * ld + col0 + col), y);
+            float4* dst = reinterpret_cast<float4*>(out + (size_t)t * ld + col0 + col);
+            if (first) *dst = y;
+            else atomicAdd(dst, y);
         }
     }
     __syncwarp();
 }
 
-// Combine: token and gate of tile row `r` (lane's row of the warp's block), or (0, 0)
-// past the tile's rows.
-__device__ __forceinline__ void combine_row(const DispatchGemmParams& p, int row0, int r, int rows,
-                                            int& tok, float& w) {
-    tok = 0;
-    w = 0.f;
+// Combine: token, gate and order of tile row `r` (this lane's row), or (0, 0, 1) past
+// the tile's rows.  The row is its token's first contribution when no other slot of the
+// token has a lower destination row (destination rows are expert-major, so that slot's
+// expert would be lower).
+__device__ __forceinline__ CombineRow combine_row(const DispatchGemmParams& p, int row0, int r, int rows) {
+    CombineRow c{0, 0.f, 1};
     if (r < rows) {
-        const int s = __ldg(p.perm + row0 + r);
-        tok = s / p.k;
-        w = __ldg(p.topk_w + s);
+        const int row = row0 + r;
+        const int s = __ldg(p.perm + row);
+        c.tok = s / p.k;
+        c.w = __ldg(p.topk_w + s);
+        for (int j = 0; j < p.k; ++j)
+            if (__ldg(p.dest + c.tok * p.k + j) < row) c.first = 0;
     }
+    return c;
+}
+
+// Combine completion word of column tile n of the 128-row tile `mtile`: word 0, or for an
+// M=128 pair tile (whose two CTAs each hold 64 of its rows) word `half` of that CTA.
+__device__ __forceinline__ uint32_t* combine_flag(const DispatchGemmParams& p, int mtile, int n, int half) {
+    return p.cflags + ((size_t)mtile * p.n_tiles + n) * 2 + half;
+}
+
+// Waits (this lane) until every lower contribution of the token of tile row `r` to
+// column tile n has landed: for each other slot of the token whose destination row r2
+// is below this row, the completion word of r2's 128-row tile (or, for an M=128 pair
+// tile, of r2's 64-row half) in column tile n holds the call's epoch.  Such tiles
+// belong to lower experts and were claimed earlier, so the wait always ends; it is
+// still bounded (MOE_ERR_TIMEOUT, then the row proceeds).
+__device__ void combine_wait_lower(const DispatchGemmParams& p, const int* mt_base, bool pair, int row0, int r,
+                                   int rows, int n, const CombineRow& c, const Waiter& w) {
+    if (r >= rows || c.first) return;
+    const int row = row0 + r;
+    for (int j = 0; j < p.k; ++j) {
+        const int r2 = __ldg(p.dest + c.tok * p.k + j);
+        if (r2 >= row) continue;
+        int lo = 0, hi = p.E;  // the expert holding r2: the largest e with offsets[e] <= r2
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.offsets + mid) <= r2) lo = mid;
+            else hi = mid;
+        }
+        const int seg = __ldg(p.offsets + lo);
+        const int lt = (r2 - seg) / kTileM;
+        int half = 0;
+        if (pair) {
+            const int cnt = __ldg(p.offsets + lo + 1) - seg;
+            if (cnt - 2 * kTileM * (lt >> 1) <= kTileM) half = (r2 - seg - kTileM * lt) >= kTileM / 2 ? 1 : 0;
+        }
+        const uint32_t* f = combine_flag(p, mt_base[lo] + lt, n, half);
+        if (ld_acquire_gpu(f) == w.epoch) continue;
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (ld_acquire_gpu(f) == w.epoch) break;
+            if ((i & 31u) == 0 && global_timer_ns() - t0 > (uint64_t)w.flag_timeout_ns) {
+                report_error(w.status, kStTimeout, -4, row, (int)w.epoch);
+                break;
+            }
+        }
+    }
+}
+
+// After a tile's combine stores: every epilogue thread fences its stores and reductions,
+// the four epilogue warps meet at named barrier 1, and one thread releases the tile's
+// completion word for column tile n with the call's epoch.
+__device__ __forceinline__ void combine_publish(const DispatchGemmParams& p, int mtile, int n, int half,
+                                               uint32_t epoch) {
+    __threadfence();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (threadIdx.x == kEpiWarp0 * 32 && mtile >= 0) st_release_gpu(combine_flag(p, mtile, n, half), epoch);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -551,7 +620,8 @@ __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.f + ex
 // goes 64 columns at a time, packed into 32 words per row, so that it leaves
 // through the same full-line (128-byte) row stores as a 32-column fp32 block.
 __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const TileInfo& ti, int bn,
-                                              uint32_t tbase, int q, int lane, float* epi) {
+                                              uint32_t tbase, int q, int lane, float* epi,
+                                              const CombineRow& cr) {
     const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
     if (p.glu) {
         const int half = bn / 2;
@@ -595,15 +665,12 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
         }
     } else if (p.combine) {
         const int ncols = min(bn, p.N - ti.n * bn);
-        int tok;
-        float w;
-        combine_row(p, ti.row0, 32 * q + lane, ti.rows, tok, w);
         for (int c = 0; c < ncols; c += 32) {
             uint32_t v[32];
             tmem_ld_32x32(tbase + (uint32_t)c, v);
             tmem_ld_wait(v);
             if (rows_valid > 0)
-                red_block_rows(epi, v, p.out, (size_t)p.N, ti.n * bn + c, rows_valid, ncols - c, lane, tok, w);
+                red_block_rows(epi, v, p.out, (size_t)p.N, ti.n * bn + c, rows_valid, ncols - c, lane, cr);
         }
     } else {
         float* ybase = static_cast<float*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
@@ -625,15 +692,13 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
 // address.  Not used for gated tiles, whose gate and up columns would then lie
 // in different warps.
 __device__ __forceinline__ void epilogue_tile_m128(const DispatchGemmParams& p, const TileInfo& ti, int bn,
-                                                   uint32_t tacc, int q, int lane, float* epi) {
+                                                   uint32_t tacc, int q, int lane, float* epi,
+                                                   const CombineRow& cr) {
     const int rb = q & 1, ch = q >> 1;
     const int rows_valid = min(32, ti.rows - 32 * rb);
     if (rows_valid <= 0) return;  // warp-uniform
     const uint32_t tq = tacc + ((uint32_t)(32 * q) << 16);
     const size_t row = (size_t)(ti.row0 + 32 * rb);
-    int tok = 0;
-    float wgt = 0.f;
-    if (p.combine) combine_row(p, ti.row0, 32 * rb + lane, ti.rows, tok, wgt);
     for (int h = 0; h < bn / 256; ++h) {
         const int col0 = ti.n * bn + 256 * h + 128 * ch;  // first Y column of this warp's block
         const int ncols = min(128, p.N - col0);
@@ -660,7 +725,7 @@ __device__ __forceinline__ void epilogue_tile_m128(const DispatchGemmParams& p, 
                 uint32_t v[32];
                 tmem_ld_32x32(t0 + (uint32_t)c, v);
                 tmem_ld_wait(v);
-                red_block_rows(epi, v, p.out, (size_t)p.N, col0 + c, rows_valid, ncols - c, lane, tok, wgt);
+                red_block_rows(epi, v, p.out, (size_t)p.N, col0 + c, rows_valid, ncols - c, lane, cr);
             }
         } else {
             float* ybase = static_cast<float*>(p.Y) + row * p.N + col0;
@@ -859,18 +924,26 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
-            // the last k-block of a reduction that is not a multiple of 64 stops at d: the
-            // loaded columns past d (zero-filled A, the next expert's W rows) are not used
-            const int ksteps = kb == p.k_blocks - 1 ? p.last_ksteps : kTileK / kUmmaK;
+            // The common k-block issues its four MMAs straight (the MMA thread's issue latency
+            // is on the critical path); a last k-block of a reduction that is not a multiple
+            // of 64 stops at d: the loaded columns past d (zero-filled A, the next expert's W
+            // rows) are not used.
+            // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
+            // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
+            //    1024 B apart (SBO); K step of 16 rows = +2048 B.
+            if (kb != p.k_blocks - 1 || p.last_ksteps == kTileK / kUmmaK) {
 #pragma unroll
-            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
-                if (kk >= ksteps) break;
-                // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
-                // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
-                //    1024 B apart (SBO); K step of 16 rows = +2048 B.
-                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                    umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+            } else {
+                for (int kk = 0; kk < p.last_ksteps; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                    umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                }
             }
             umma_commit(smem_addr(&ctl->empty[stage]));
             if (++stage == STAGES) {
@@ -890,7 +963,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
 
 template <int BN, int STAGES>
 __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
-                              const Waiter& w, float* epi) {
+                              const Waiter& w, float* epi, const int* mt_base) {
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter of this warp
     int slot = 0;
@@ -911,36 +984,47 @@ __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 9);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
+        CombineRow cr{0, 0.f, 1};
+        if (p.combine) {
+            cr = combine_row(p, ti.row0, 32 * q + lane, ti.rows);
+            combine_wait_lower(p, mt_base, false, ti.row0, 32 * q + lane, ti.rows, ti.n, cr, w);
+            __syncwarp();
+        }
         const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(32 * q) << 16);
-        epilogue_tile(p, ti, BN, tbase, q, lane, epi);
+        epilogue_tile(p, ti, BN, tbase, q, lane, epi, cr);
         tc_fence_before();
         mbar_arrive(smem_addr(&ctl->tempty[acc]));
+        if (p.combine) combine_publish(p, ti.mtile, ti.n, 0, w.epoch);
         acc ^= 1;
         if (acc == 0) aphase ^= 1u;
     }
 }
 
-// Direct-gather A loads (gather mode, warps 2 and 3): for every tile the warps
-// take from the schedule ring, warp `part` copies the tile's rows
-// [64 part, 64 part + 64) straight from their token rows of x (perm[row] / k)
-// into the stage's A buffer with 16-byte cp.async, in the 128-byte-swizzled
-// K-major layout the MMA descriptors expect (16-byte chunk c of row r lands at
-// r*128 + (c ^ (r%8))*16).  Eight lanes cover one row's 128 bytes of a k-block,
-// so each copy instruction moves four whole 128-byte lines.  Rows past the
-// tile's valid rows are zero-filled.  Each warp keeps up to STAGES-2 stages of
-// copies in flight; once a stage's copies are complete it fences them for the
-// async proxy (the tensor cores read shared memory there) and arrives on the
-// stage's full barrier, which also waits for the other warp and the TMA
-// thread's B bytes.  No receive buffer is written and no ready flag is read.
-// The copies are plain 16-byte cp.async rather than TMA: a TMA copy per
-// gathered row (or tile::gather4) would write single rows into the middle of
-// the 1024-byte swizzle atom, a placement this kernel does not rely on.
+// Direct-gather A loads (gather mode, warps 2 and 3 of every CTA): for every tile
+// the warps take from the schedule ring, warp `part` copies the CTA's rows
+// [64 part, 64 part + 64) of the tile straight from their token rows of x
+// (perm[row] / k) into the stage's A buffer with 16-byte cp.async, in the
+// 128-byte-swizzled K-major layout the MMA descriptors expect (16-byte chunk c of
+// row r lands at r*128 + (c ^ (r%8))*16).  Eight lanes cover one row's 128 bytes of
+// a k-block, so each copy instruction moves four whole 128-byte lines.  Rows past
+// the tile's valid rows are zero-filled.  Each warp keeps up to STAGES-2 stages of
+// copies in flight; once a stage's copies are complete it fences them for the async
+// proxy (the tensor cores read shared memory there) and arrives on the stage's full
+// barrier, which also waits for the other gather warps and the B bytes.  In CTA
+// pairs that is the leader's barrier: the peer's warps arrive on it remotely
+// (release at cluster scope), since the leader's MMAs read both CTAs' rows.  No
+// receive buffer is written and no ready flag is read.  In CTA pairs the peer's
+// gather warps arrive on the peer's own `afull` barrier, and the peer's relay thread
+// (pair_relay_role) passes each completed stage on to the leader's stage barrier.
+// The copies are cp.async by warps, not TMA: a TMA gather of four 128-byte rows
+// (tile::gather4) per lane ran about 3x slower than this here (32 small TMA
+// operations per k-block and CTA).
 constexpr int kGatherWarp0 = 2;
 constexpr int kGatherWarps = 2;
 constexpr int kGatherRows = kTileM / kGatherWarps;  // rows per warp
 template <int STAGES>
 __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, const Waiter& w,
-                              int part) {
+                              int part, bool pair, bool leader, uint32_t lead) {
     constexpr int kABytes = kTileM * kTileK * 2;  // 128 rows x 64 columns
     constexpr int kLag = STAGES - 2 >= 1 ? STAGES - 2 : 1;  // stages in flight before an arrive
     constexpr int kIters = kGatherRows / 4;
@@ -957,22 +1041,26 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         cp_async_wait_dyn(keep);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl->full[pend[head]]));
+        if (lane == 0) mbar_arrive(smem_addr(leader ? &ctl->full[pend[head]] : &ctl->afull[pend[head]]));
         head = head + 1 == kMaxStages ? 0 : head + 1;
         --npend;
     };
     bool ok = true;
     while (ok) {
-        const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 40);
+        const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 40, true, pair);
         if (!__all_sync(kFull, got)) break;
         const TileInfo ti = ctl->ring[slot];
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (lane == 0) {
+            const uint32_t se = smem_addr(&ctl->sempty[slot]);
+            if (leader) mbar_arrive(se);
+            else mbar_arrive_cluster(mapa_shared(se, lead));
+        }
         if (++slot == kRing) {
             slot = 0;
             sphase ^= 1u;
         }
-        if (ti.rows < 0) break;
+        if (pair ? ti.e < 0 : ti.rows < 0) break;
         // this lane copies chunk c of the warp's rows 4i + lane/8 (i < 16): their
         // token rows, gathered from the lanes that read perm, stay in registers
         const int c = lane & 7;
@@ -994,7 +1082,7 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
             bool free_ok = true;
-            if (lane == 0) free_ok = wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 41);
+            if (lane == 0) free_ok = wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 41, true, pair);
             if (!__shfl_sync(kFull, free_ok ? 1 : 0, 0)) {
                 ok = false;
                 break;
@@ -1026,6 +1114,37 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     // every copy lands and is published before the CTA can leave (also on abort,
     // so that the TMA thread's drain of the full barriers ends)
     while (npend > 0) retire_oldest(0);
+}
+
+// Gather mode, peer CTA of a pair (its otherwise idle warp 1, lane 0): follows the
+// schedule ring and, for every stage, waits until the peer's gather warps have landed
+// their A rows (the peer's `afull` barrier) and then arrives on the leader's stage
+// barrier, which the leader's MMA thread waits on.  One cluster-scope arrival per
+// stage from this thread, instead of one from each gather warp.
+template <int STAGES>
+__device__ void pair_relay_role(const DispatchGemmParams& p, SmemCtl* ctl, const Waiter& w, uint32_t lead) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    for (;;) {
+        if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 31, true, true)) return;
+        const int e = ctl->ring[slot].e;
+        mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (e < 0) return;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->afull[stage]), phase, w, 32, true, true)) return;
+            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->full[stage]), lead));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
 }
 
 template <int BN, int STAGES>
@@ -1112,9 +1231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mma_role<BN, STAGES>(p, ctl, sA, sB, tmem_base, w);
         __syncwarp();
     } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
-        gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0);
+        gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0, false, true, 0);
     } else if (warp >= kEpiWarp0) {
-        epilogue_role<BN, STAGES>(p, ctl, tmem_base, w, epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
+        epilogue_role<BN, STAGES>(p, ctl, tmem_base, w, epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats, mt_base);
     }
 
     tc_fence_before();
@@ -1235,7 +1354,8 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     using C = PairCfg<STAGES, BN>;
     const uint32_t total_tiles = (uint32_t)pt_base[p.E] * (uint32_t)p.n_tiles;
     tma_prefetch_map(&p.b_map);
-    for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
+    if (!p.gather)  // no A tensor map in the gather mode
+        for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
     const uint32_t lead = leader ? cluster_ctarank() : peer;  // rank of the leader CTA
     int stage = 0;
     uint32_t phase = 0;
@@ -1293,7 +1413,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             slot = 0;
             sphase ^= 1u;
         }
-        flag = (ti.e >= 0 && ti.rows > 0 && !p.a_ready) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        flag = (ti.e >= 0 && ti.rows > 0 && !p.a_ready && !p.gather) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
         got = true;
         return true;
     };
@@ -1347,8 +1467,12 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             }
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
-            if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
-            tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
+            if (p.gather) {  // both CTAs' gather warps fill A and arrive on this barrier
+                if (leader) mbar_arrive_expect_tx(fb_local, 2u * 8192u * (uint32_t)nbox);
+            } else {
+                if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
+                tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
+            }
 #pragma unroll
             for (int b = 0; b < 2 * C::kHalves; ++b)
                 if (b < nbox)
@@ -1409,15 +1533,24 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
-            const int ksteps = kb == p.k_blocks - 1 ? p.last_ksteps : kTileK / kUmmaK;  // stop at d
+            if (kb != p.k_blocks - 1 || p.last_ksteps == kTileK / kUmmaK) {  // as in the single-CTA kernel
 #pragma unroll
-            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
-                if (kk >= ksteps) break;
-                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
-                    const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
-                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
+                        const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
+                        umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                }
+            } else {  // stop at d
+                for (int kk = 0; kk < p.last_ksteps; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
+                        umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
                 }
             }
             umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
@@ -1439,7 +1572,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
 
 template <int STAGES, int BN>
 __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_t tmem_base,
-                                   const Waiter& w, bool leader, uint32_t lead, float* epi) {
+                                   const Waiter& w, bool leader, uint32_t lead, float* epi, const int* mt_base) {
     using C = PairCfg<STAGES, BN>;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
@@ -1465,11 +1598,18 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         const bool ready = wait_bar(smem_addr(&ctl->tfull[acc]), aphase, w, 30, true, true);
         if (!__all_sync(kFull, ready)) break;
         tc_fence_after();
+        CombineRow cr{0, 0.f, 1};
+        if (p.combine) {  // this warp's rows: 32 q + lane, or 32 (q & 1) + lane of an M=128 half
+            const int r = ti.m128 ? 32 * (q & 1) + lane : 32 * q + lane;
+            cr = combine_row(p, ti.row0, r, ti.rows);
+            combine_wait_lower(p, mt_base, true, ti.row0, r, ti.rows, ti.n, cr, w);
+            __syncwarp();
+        }
         if (ti.m128) {
-            epilogue_tile_m128(p, ti, C::kBN, tmem_base + (uint32_t)(acc * C::kBN), q, lane, epi);
+            epilogue_tile_m128(p, ti, C::kBN, tmem_base + (uint32_t)(acc * C::kBN), q, lane, epi, cr);
         } else if (ti.rows - 32 * q > 0) {  // the odd half of a pair tile may hold fewer rows
             const uint32_t tbase = tmem_base + (uint32_t)(acc * C::kBN) + ((uint32_t)(32 * q) << 16);
-            epilogue_tile(p, ti, C::kBN, tbase, q, lane, epi);
+            epilogue_tile(p, ti, C::kBN, tbase, q, lane, epi, cr);
         }
         tc_fence_before();
         __syncwarp();
@@ -1478,6 +1618,8 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
             if (leader) mbar_arrive(te);
             else mbar_arrive_cluster(mapa_shared(te, lead));
         }
+        if (p.combine)  // an M=128 tile's two CTAs each publish their 64-row half
+            combine_publish(p, ti.rows > 0 ? ti.mtile : -1, ti.n, ti.m128 ? (leader ? 0 : 1) : 0, w.epoch);
         if (++acc == C::kAccs) {
             acc = 0;
             aphase ^= 1u;
@@ -1507,7 +1649,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lead = rank & ~1u;
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_addr(&ctl->full[s]), 1);   // leader: its expect_tx arrival + both CTAs' bytes
+            // leader: its expect_tx arrival + both CTAs' bytes (+ its gather warps and the
+            // peer's relay in the gather mode); peer's afull: its gather warps
+            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + kGatherWarps + 1 : 1);
+            mbar_init(smem_addr(&ctl->afull[s]), kGatherWarps);
             mbar_init(smem_addr(&ctl->empty[s]), 1);  // the leader's multicast commit
         }
         for (int a = 0; a < 2; ++a) {
@@ -1516,8 +1661,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(smem_addr(&ctl->sfull[r]), 1);
-            // leader: own MMA thread + 4 epilogue warps + the peer's TMA thread and 4 epilogue warps
-            mbar_init(smem_addr(&ctl->sempty[r]), 10);
+            // leader: own MMA thread + 4 epilogue warps + the peer's TMA thread and 4 epilogue
+            // warps (+ both CTAs' gather warps and the peer's relay in the gather mode)
+            mbar_init(smem_addr(&ctl->sempty[r]), 10 + (p.gather ? 2 * kGatherWarps + 1 : 0));
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -1579,10 +1725,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && leader) pair_mma_role<STAGES, BN>(p, ctl, sA, sB, tmem_base, w);
+        else if (lane == 0 && p.gather) pair_relay_role<STAGES>(p, ctl, w, lead);
         __syncwarp();
+    } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
+        gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0, true, leader, lead);
     } else if (warp >= kEpiWarp0) {
         pair_epilogue_role<STAGES, BN>(p, ctl, tmem_base, w, leader, lead,
-                                   epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats);
+                                   epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats, mt_base);
     }
 
     tc_fence_before();

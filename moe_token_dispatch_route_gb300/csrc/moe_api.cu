@@ -29,7 +29,7 @@ struct moe_plan_s {
     int skip_publish = -1;
     int band = 0;
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
-    bool single_ready = false;  // pair plans: single-CTA kernel attributes set (direct gather)
+    bool single_ready = false;  // automatic pair plans: single-CTA kernel attributes set (direct gather)
     unsigned long long* trace = nullptr;  // per-CTA trace records (moe_set_trace), or null
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
@@ -246,6 +246,8 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     off = round_up(off + (size_t)p->max_mtiles * 4, 256);
     p->ws.chunk_cnt_off = off;
     off = round_up(off + (size_t)p->max_mtiles * 4, 256);
+    p->ws.cflags_off = off;
+    off = round_up(off + (size_t)p->max_mtiles * ((p->N + kTileM - 1) / kTileM) * 2 * 4, 256);
     p->ws.total = off;
 
     if ((!p->pair && dispatch_gemm_prepare_attributes(p->tile_n, p->stages, p->smem) != cudaSuccess) ||
@@ -347,18 +349,18 @@ enum class GemmMode { kDispatch, kDispatchSwiglu, kGrouped, kGather, kDispatchCo
 moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const int32_t* offsets,
                       const int32_t* perm, const uint16_t* W, void* const* recv, const uint16_t* A,
                       void* Y, uint16_t* H, void* workspace, int32_t* dev_status, void* stream,
-                      const float* topk_w = nullptr, float* out = nullptr) {
+                      const int32_t* dest = nullptr, const float* topk_w = nullptr, float* out = nullptr) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return MOE_ERR_WORKSPACE;
     const bool glu = mode == GemmMode::kDispatchSwiglu;
     const bool combine = mode == GemmMode::kDispatchCombine;
     if (glu && plan->tile_n == 192) return MOE_ERR_UNSUPPORTED;  // halves must be whole 64-column boxes
-    if (combine && plan->k > 2) return MOE_ERR_UNSUPPORTED;      // reproducible for k <= 2 only
     if (plan->T == 0) return MOE_OK;
     if (!offsets || !W || !aligned(W, 16) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
     if (combine) {
-        if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+        if (!dest || !topk_w || !out || !aligned(dest, 4) || !aligned(topk_w, 4) || !aligned(out, 16))
+            return MOE_ERR_INVALID_ARG;
     } else if (glu ? (!H || !aligned(H, 16)) : (!Y || !aligned(Y, 16))) {
         return MOE_ERR_INVALID_ARG;
     }
@@ -415,6 +417,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.out_bf16 = (!combine && plan->shape.out_dtype == MOE_OUT_BF16) ? 1 : 0;
     prm.combine = combine ? 1 : 0;
     prm.topk_w = topk_w;
+    prm.dest = dest;
     prm.out = out;
     prm.trace = plan->trace;
     prm.H = H;
@@ -425,6 +428,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.hdr = reinterpret_cast<uint32_t*>(ws);
     prm.flags = reinterpret_cast<uint32_t*>(ws + plan->ws.flags_off);
     prm.chunk_cnt = reinterpret_cast<uint32_t*>(ws + plan->ws.chunk_cnt_off);
+    prm.cflags = reinterpret_cast<uint32_t*>(ws + plan->ws.cflags_off);
     prm.status = dev_status;
     prm.timeout_ns = plan->timeout_ns;
     prm.T = plan->T;
@@ -445,14 +449,11 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
     cudaError_t lerr;
-    if (combine &&
-        cudaMemsetAsync(out, 0, (size_t)plan->T * plan->N * sizeof(float), static_cast<cudaStream_t>(stream)) !=
-            cudaSuccess) {
-        cudaGetLastError();
-        return MOE_ERR_CUDA;
-    }
-    if (gather && plan->pair) {
-        // the direct gather runs in the single-CTA kernel: 256-wide tiles, 4 stages
+    if (gather && plan->pair && plan->shape.tile_m != 256) {
+        // The direct gather of an automatic pair plan runs in the single-CTA kernel with
+        // 256-wide tiles: there it moves its rows about twice as fast as on CTA pairs, whose
+        // peer must signal every gathered stage to the leader across the pair.  A plan that
+        // asks for CTA pairs (tile_m = 256) gets the pair version.
         const size_t smem = dispatch_gemm_smem_bytes(256, 4);
         {
             std::lock_guard<std::mutex> lock(plan->mu);
@@ -494,11 +495,11 @@ moe_status_t moe_dispatch_gemm(moe_plan_t plan, const uint16_t* x, const int32_t
 }
 
 moe_status_t moe_dispatch_gemm_combine(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,
-                                       const int32_t* perm, const float* topk_w, const uint16_t* W,
-                                       void* const* recv, float* out, void* workspace, int32_t* dev_status,
-                                       void* stream) {
+                                       const int32_t* perm, const int32_t* dest, const float* topk_w,
+                                       const uint16_t* W, void* const* recv, float* out, void* workspace,
+                                       int32_t* dev_status, void* stream) {
     return run_gemm(plan, GemmMode::kDispatchCombine, x, offsets, perm, W, recv, nullptr, nullptr, nullptr,
-                    workspace, dev_status, stream, topk_w, out);
+                    workspace, dev_status, stream, dest, topk_w, out);
 }
 
 moe_status_t moe_dispatch_gemm_swiglu(moe_plan_t plan, const uint16_t* x, const int32_t* offsets,

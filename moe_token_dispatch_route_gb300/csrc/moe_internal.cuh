@@ -46,6 +46,7 @@ struct WorkspaceLayout {
     size_t route_blk_off;   // int32 [route_blocks][E]
     size_t flags_off;       // u32 [max_mtiles]
     size_t chunk_cnt_off;   // u32 [max_mtiles]
+    size_t cflags_off;      // u32 [max_mtiles][ceil(N / 128)][2] combine completion words (epoch-tagged)
     size_t total;
 };
 
@@ -104,10 +105,13 @@ struct DispatchGemmParams {
     int gather;                     // 1: A rows are copied from x by perm into shared memory
                                     //    (no receive buffers, no scatter, no flags)
     int out_bf16;                   // 1: Y is bf16 (fp32 accumulator rounded once)
-    int combine;                    // 1: no Y; each row, times its slot's gate, is added into
-                                    //    its token's row of `out` (zeroed before the launch)
+    int combine;                    // 1: no Y; each row, times its slot's gate, goes into its
+                                    //    token's row of `out`: stored by the token's lowest
+                                    //    expert, then added by the others in expert order
     const float* topk_w;            // combine: [T*k] gate of each slot
+    const int32_t* dest;            // combine: [T*k] destination row of each slot
     float* out;                     // combine: fp32 [T][N]
+    uint32_t* cflags;               // combine: u32 [max_mtiles][n_tiles][2] tile completion words
     unsigned long long* trace;      // [grid][kTraceWords] per-CTA stamps, or null (off)
 };
 

@@ -1,7 +1,8 @@
 """Direct-gather grouped GEMM (moe_gather_gemm) on the GPU.
 
 The A rows come straight from x (row perm[i] / k for destination row i) into
-the GEMM's shared-memory tiles; no receive buffer is written.  Each output
+the GEMM's shared-memory tiles by 16-byte asynchronous copies; no receive buffer
+is written.  Each output
 element is reduced in the same order as in moe_dispatch_gemm with the same
 tile shape, so the two agree bit for bit; both are also checked against the
 oracle.
@@ -67,27 +68,34 @@ def test_gather_other_tile_widths(tile_n):
     assert torch.equal(Y_gather, bufs.Y)
 
 
-@pytest.mark.parametrize("T,d,E,k,N", [
-    (1500, 128, 4, 2, 512),     # several 256-row tiles per expert
-    (1000, 128, 2, 1, 400),     # ragged column tail
+@pytest.mark.parametrize("T,d,E,k,N,tile_n", [
+    (1500, 128, 4, 2, 512, 256),     # several 256-row pair tiles per expert, M=128 tails
+    (1000, 128, 2, 1, 400, 256),     # ragged column tail
+    (1200, 128, 4, 2, 1408, 256),    # an N=128 last column tile
+    (1000, 80, 2, 2, 1040, 512),     # 512-wide pair tiles, d = 80
+    (130, 64, 1, 1, 256, 256),       # one expert of 130 rows: an M=128 tail after a full half
 ])
-def test_gather_on_a_pair_plan_uses_256_wide_single_tiles(T, d, E, k, N):
-    """A CTA-pair plan runs the gather in the single-CTA kernel with 256-wide
-    tiles: bit for bit the single-CTA dispatch with tile_n = 256."""
+def test_gather_on_cta_pairs_matches_dispatch_bitwise(T, d, E, k, N, tile_n):
+    """CTA-pair plans gather on CTA pairs (the peer's gather warps arrive on the leader's
+    stage barrier): bit for bit the pair dispatch with the same tiles, and the oracle."""
     wl = workloads.custom("gpair", T, d, E, k, N, 1, "none")
     inp = workloads.make_inputs(wl, seed=22)
-    plan, bufs, Y_gather = _both(wl, inp, tile_m=256)
+    plan, bufs, Y_gather = _both(wl, inp, tile_m=256, tile_n=tile_n)
     assert plan.info["tile_m"] == 256
-    _, bufs1, _ = _both(wl, inp, tile_m=128, tile_n=256)
-    assert torch.equal(Y_gather, bufs1.Y)
+    assert torch.equal(Y_gather, bufs.Y)
+    ref = oracle.route(inp["logits"].numpy(), k)
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], k)
+    check_Y(Y_gather.cpu().double().numpy(),
+            oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"]))
 
 
 def test_gather_repeated_calls_and_grid_sizes():
     wl = workloads.custom("grep", 900, 256, 8, 2, 512, 2, "none")
     inp = workloads.make_inputs(wl, seed=23)
     outs = []
-    for kw in (dict(), dict(num_ctas=16), dict(num_ctas=3)):
-        plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, tile_m=128, **kw)
+    for kw in (dict(tile_m=128), dict(tile_m=128, num_ctas=16), dict(tile_m=128, num_ctas=3),
+               dict(tile_m=256), dict(tile_m=256, num_ctas=6), dict(tile_m=256, num_ctas=2)):
+        plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, num_ranks=wl.R, **kw)
         bufs = binding.MoeBuffers(plan, "cuda")
         x, W, L = inp["x"].cuda(), inp["W"].cuda(), inp["logits"].cuda()
         binding.route(plan, L, bufs)
@@ -97,14 +105,17 @@ def test_gather_repeated_calls_and_grid_sizes():
             rc, status = binding.moe_read_status(bufs.status)
             assert rc == 0, status
             outs.append(bufs.Y.clone())
-    for o in outs[1:]:
+    for o in outs[1:4]:
         assert torch.equal(outs[0], o)
+    for o in outs[4:]:  # CTA pairs: the same K order per element, the M=256 MMA's own rounding
+        assert torch.equal(outs[3], o)
 
 
 @pytest.mark.parametrize("name", ["mixtral", "finegrained", "deepseek_v3", "decode"])
 def test_gather_full_size(name):
-    """In the launch configuration of the benchmark (the plan's own choice);
-    bit for bit against the single-CTA dispatch with the same tiles."""
+    """In the launch configuration of the benchmark (the plan's own choice: an
+    automatic pair plan gathers in 256-wide single-CTA tiles); bit for bit against
+    the dispatch where the tile shapes agree."""
     wl = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
     plan, bufs, Y_gather = _both(wl, inp)
