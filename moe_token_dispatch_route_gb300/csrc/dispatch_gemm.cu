@@ -59,8 +59,6 @@ struct TileInfo {
     int arow;  // first row inside the rank's receive buffer
     int m128;  // CTA pairs: 1 for an expert's last tile of at most 128 rows, run as an
                // M=128 pair MMA (64 rows per CTA); 0 otherwise
-    int narrow;  // CTA pairs, 256-wide tiles: 1 for a last column tile of at most 128
-                 // columns, run as an N=128 pair MMA; 0 otherwise
 };
 
 constexpr int kMaxPieceBufs = 8;
@@ -149,19 +147,25 @@ __device__ void wait_flag(const uint32_t* flag, const Waiter& w, int mtile, int 
     }
 }
 
-// Per-expert ceil(count / div) -> exclusive prefix table[0..E] (E <= 1024), all threads.
-__device__ void build_expert_table(const int32_t* offsets, int E, int div, int* table, int* wsum) {
+// Exclusive prefix table[0..nch E] (nch E <= 1024) of per-(chunk, expert) counts, all
+// threads.  With U_e = ceil(count_e / div), entry c E + e counts the part
+// [floor(c U_e / nch), floor((c+1) U_e / nch)) of expert e's U_e items: chunk-major
+// order, nch = 1 giving the per-expert ceil(count / div) prefix.
+__device__ void build_expert_table(const int32_t* offsets, int E, int div, int* table, int* wsum, int nch = 1) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int base = tid * 4;
+    const int n = nch * E;
     int loc[4];
     int sum = 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int e = base + u;
+        const int i = base + u;
         int v = 0;
-        if (e < E) {
+        if (i < n) {
+            const int c = i / E, e = i - c * E;
             const int cnt = __ldg(offsets + e + 1) - __ldg(offsets + e);
-            v = (cnt + div - 1) / div;
+            const long long U = (cnt + div - 1) / div;
+            v = (int)((c + 1) * U / nch - c * U / nch);
         }
         loc[u] = v;
         sum += v;
@@ -182,10 +186,10 @@ __device__ void build_expert_table(const int32_t* offsets, int E, int div, int* 
     int run = pre + incl - sum;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        if (base + u < E) table[base + u] = run;
+        if (base + u < n) table[base + u] = run;
         run += loc[u];
     }
-    if (tid == 0) table[E] = total;
+    if (tid == 0) table[n] = total;
     __syncthreads();
 }
 
@@ -204,10 +208,14 @@ __device__ __forceinline__ int expert_of(const int* table, int E, int u) {
 // receive buffers.
 //
 // Work unit = up to 4 consecutive destination rows of one expert inside one
-// 128-row tile; only non-empty units exist (unit_base holds the per-expert
-// prefix of ceil(count/4)).  Units are visited in destination order, strided
-// over all scatter warps of all scatter CTAs, so the earliest tiles fill
-// first.  Each row is split into pieces of at most 512 16-byte vectors.
+// 128-row tile; only non-empty units exist.  Units are visited strided over all
+// scatter warps of all scatter CTAs in chunk-major order: each expert's units are
+// cut into p.nch equal parts (unit_base holds the prefix over (part, expert)), and
+// part c of every expert comes before part c+1 of any.  An expert's rows are in token
+// order, so part c of every expert holds about the same c-th slice of the tokens,
+// and the k copies of a token row are read while its x row is still in L2 (one DRAM
+// read per token row instead of up to k).  Each row is split into pieces of at most
+// 512 16-byte vectors.
 //
 // The loads are cp.async.cg (global -> shared, no L1 allocation) into a
 // lane-private staging area carved from the idle GEMM stage buffers (24 KB
@@ -258,10 +266,13 @@ __device__ void cursor_fetch_batch(UnitCursor& u, const DispatchGemmParams& p, c
         u.m_local[r] = -1;
     }
     if (c >= u.total) return;
-    const int e = expert_of(unit_base, p.E, c);
-    const int j = c - unit_base[e];
+    const int i = expert_of(unit_base, p.nch * p.E, c);  // (part, expert) holding unit c
+    const int part = i / p.E;
+    const int e = i - part * p.E;
     const int seg0 = __ldg(p.offsets + e);
     const int cnt = __ldg(p.offsets + e + 1) - seg0;
+    const long long U = (cnt + kRowsPerChunk - 1) / kRowsPerChunk;
+    const int j = (int)(part * U / p.nch) + (c - unit_base[i]);  // unit index inside the expert
     const int e_per_rank = p.E / p.R;
     const int rank = e / e_per_rank;
     const int rbase = __ldg(p.offsets + rank * e_per_rank);
@@ -306,7 +317,7 @@ __device__ void cursor_init(UnitCursor& u, const DispatchGemmParams& p, const in
                             int stride, uint32_t epoch, int lane) {
     u.c = first;
     u.stride = stride;
-    u.total = unit_base[p.E];
+    u.total = unit_base[p.nch * p.E];
     u.slot = 0;
     cursor_fetch_batch(u, p, unit_base, epoch, lane);
     cursor_select(u);
@@ -798,7 +809,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
         const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
         if (tile >= total_tiles) {
-            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = ti.narrow = 0;
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = 0;
             ti.rows = -1;
         } else {
             const int u = (int)(tile / (uint32_t)p.n_tiles);
@@ -823,7 +834,6 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             ti.rank = e / e_per_rank;
             ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
             ti.m128 = 0;
-            ti.narrow = 0;
         }
         ctl->ring[slot] = ti;
         mbar_arrive(smem_addr(&ctl->sfull[slot]));
@@ -916,7 +926,12 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
         if (!wait_bar(smem_addr(&ctl->tempty[acc]), aphase ^ 1u, w, 5)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // k-blocks of four K=16 steps in the loop; a last k-block of a reduction that is
+        // not a multiple of 64 (fewer steps: the loaded columns past d, zero-filled A and the
+        // next expert's W rows, are not used) after it, so that the loop body stays lean:
+        // the MMA thread's issue latency is on the critical path
+        const int kfull = p.last_ksteps == kTileK / kUmmaK ? p.k_blocks : p.k_blocks - 1;
+        for (int kb = 0; kb < kfull; ++kb) {
             if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 6)) {
                 ok = false;
                 break;
@@ -924,26 +939,30 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
-            // The common k-block issues its four MMAs straight (the MMA thread's issue latency
-            // is on the critical path); a last k-block of a reduction that is not a multiple
-            // of 64 stops at d: the loaded columns past d (zero-filled A, the next expert's W
-            // rows) are not used.
-            // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
-            // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
-            //    1024 B apart (SBO); K step of 16 rows = +2048 B.
-            if (kb != p.k_blocks - 1 || p.last_ksteps == kTileK / kUmmaK) {
 #pragma unroll
-                for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                    umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
-                }
-            } else {
-                for (int kk = 0; kk < p.last_ksteps; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                    umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
-                }
+            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                // A: K-major rows of 128 B, 8-row groups 1024 B apart; K step = +32 B.
+                // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row K groups
+                //    1024 B apart (SBO); K step of 16 rows = +2048 B.
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(smem_addr(&ctl->empty[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (ok && kfull < p.k_blocks) {  // the short last k-block
+            if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 6)) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+            const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+            for (int kk = 0; kk < p.last_ksteps; ++kk) {
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kfull | kk) != 0 ? 1u : 0u);
             }
             umma_commit(smem_addr(&ctl->empty[stage]));
             if (++stage == STAGES) {
@@ -1188,13 +1207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     build_expert_table(p.offsets, p.E, kTileM, mt_base, ctl->wsum);  // contain __syncthreads
-    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum);
+    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum, p.nch);
     if (mt_base[p.E] > p.max_mtiles || __ldg(p.offsets + p.E) != p.T * p.k) {
         // offsets that do not describe T*k rows: report, and schedule nothing
         __syncthreads();
         if (tid == 0) {
             report_error(p.status, kStDevice, -2, __ldg(p.offsets + p.E), 0);
-            for (int e = 0; e <= p.E; ++e) mt_base[e] = unit_base[e] = 0;
+            for (int e = 0; e <= p.E; ++e) mt_base[e] = 0;
+            for (int i = 0; i <= p.nch * p.E; ++i) unit_base[i] = 0;
         }
         __syncthreads();
     }
@@ -1285,10 +1305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * An expert's last tile of at most 128 rows runs as an M=128 pair MMA, 64
 //    rows per CTA, both CTAs waiting for that one row tile's flag
 //    (pair_half_info, epilogue_tile_m128).
-//  * With 256-wide tiles, a last column tile of at most 128 columns (N not a
-//    multiple of 256) runs as an N=128 pair MMA: each CTA loads one 64-column
-//    B box instead of two, and the MMA does half the work.  Not for M=128 or
-//    gated tiles.
 // The scatter role is unchanged; a pair takes one role ticket and its two
 // CTAs become scatter CTAs 2t and 2t+1.
 template <int STAGES, int BN>
@@ -1301,7 +1317,6 @@ struct PairCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 256);
     static constexpr uint32_t kIdesc128 = idesc_bf16_f32_kmajA_mnmajB(kTileM, 256);  // tail tiles
-    static constexpr uint32_t kIdescN128 = idesc_bf16_f32_kmajA_mnmajB(2 * kTileM, 128);  // narrow tiles
     static constexpr int kTmemCols = 512;                // two 256-column accumulators or one of 512
     static constexpr int kAccs = 512 / BN;               // accumulators (TMEM double buffer for 256)
     static constexpr size_t kSmem =
@@ -1347,14 +1362,14 @@ __device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, 
     ti.arow = ti.row0 - __ldg(p.offsets + ti.rank * e_per_rank);
 }
 
-template <int STAGES, int BN>
+template <int STAGES, int BN, bool GATHER>
 __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
                               const int* pt_base, uint8_t* sA, uint8_t* sB, const Waiter& w,
                               bool leader, uint32_t peer) {
     using C = PairCfg<STAGES, BN>;
     const uint32_t total_tiles = (uint32_t)pt_base[p.E] * (uint32_t)p.n_tiles;
     tma_prefetch_map(&p.b_map);
-    if (!p.gather)  // no A tensor map in the gather mode
+    if (!GATHER)  // no A tensor map in the gather mode
         for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
     const uint32_t lead = leader ? cluster_ctarank() : peer;  // rank of the leader CTA
     int stage = 0;
@@ -1377,7 +1392,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             TileInfo other;
             if (tile >= total_tiles) {
                 ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = 0;
-                ti.narrow = 0;
                 ti.e = -1;
                 other = ti;
             } else {
@@ -1389,8 +1403,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 const int m2 = local % pt_e;
                 pair_half_info(p, mt_base, e, m2, n, 0, ti);
                 pair_half_info(p, mt_base, e, m2, n, 1, other);
-                ti.narrow = other.narrow =
-                    (BN == 256 && !p.glu && !ti.m128 && p.N - n * BN <= BN / 2) ? 1 : 0;
             }
             ctl->ring[slot] = ti;
             const int* o = reinterpret_cast<const int*>(&other);
@@ -1413,7 +1425,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             slot = 0;
             sphase ^= 1u;
         }
-        flag = (ti.e >= 0 && ti.rows > 0 && !p.a_ready && !p.gather) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
+        flag = (ti.e >= 0 && ti.rows > 0 && !p.a_ready && !GATHER) ? ld_acquire_gpu(p.flags + ti.mtile) : w.epoch;
         got = true;
         return true;
     };
@@ -1445,10 +1457,6 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
             for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, cur.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
-        // a narrow tile (N=128 MMA): each CTA holds 64 of its 128 columns, box 0 or 1
-        const int nbox = cur.narrow ? 1 : 2 * C::kHalves;
-        if (cur.narrow) bcol[0] = b_box_col(p, cur.n, C::kBN, leader ? 0 : 1);
-        const uint32_t stage_tx = 2u * (uint32_t)(C::kABytes + 8192 * nbox);  // both CTAs' bytes
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -1467,17 +1475,16 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             }
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
             const uint32_t fb = mapa_shared(fb_local, lead);  // stage barrier of the leader
-            if (p.gather) {  // both CTAs' gather warps fill A and arrive on this barrier
-                if (leader) mbar_arrive_expect_tx(fb_local, 2u * 8192u * (uint32_t)nbox);
+            if (GATHER) {  // both CTAs' gather warps fill A; the barrier counts the B bytes
+                if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kBBytes);
             } else {
-                if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
+                if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
                 tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             }
 #pragma unroll
             for (int b = 0; b < 2 * C::kHalves; ++b)
-                if (b < nbox)
-                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
-                                     brow + kb * kTileK);
+                tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                 brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -1514,8 +1521,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     while (ok) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 25, true, true)) break;
         const int e = ctl->ring[slot].e;
-        const uint32_t idesc =
-            ctl->ring[slot].m128 ? C::kIdesc128 : ctl->ring[slot].narrow ? C::kIdescN128 : C::kIdesc;
+        const uint32_t idesc = ctl->ring[slot].m128 ? C::kIdesc128 : C::kIdesc;
         mbar_arrive(smem_addr(&ctl->sempty[slot]));
         if (++slot == kRing) {
             slot = 0;
@@ -1525,7 +1531,12 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         if (!wait_bar(smem_addr(&ctl->tempty[acc]), aphase ^ 1u, w, 26, true, true)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kBN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // k-blocks of four K=16 steps in the loop; a last k-block of a reduction that is
+        // not a multiple of 64 (fewer steps: the loaded columns past d are not used) after
+        // it, so the loop body stays lean (the MMA thread's issue latency is on the
+        // critical path)
+        const int kfull = p.last_ksteps == kTileK / kUmmaK ? p.k_blocks : p.k_blocks - 1;
+        for (int kb = 0; kb < kfull; ++kb) {
             if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 27, true, true)) {
                 ok = false;
                 break;
@@ -1533,24 +1544,32 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
-            if (kb != p.k_blocks - 1 || p.last_ksteps == kTileK / kUmmaK) {  // as in the single-CTA kernel
 #pragma unroll
-                for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            for (int kk = 0; kk < kTileK / kUmmaK; ++kk) {
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
-                        const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
-                        umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                for (int h = 0; h < C::kHalves; ++h) {  // tile columns [256h, 256h + 256)
+                    const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
+                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
-            } else {  // stop at d
-                for (int kk = 0; kk < p.last_ksteps; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            }
+            umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (ok && kfull < p.k_blocks) {  // the short last k-block
+            if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 27, true, true)) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+            const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+            for (int kk = 0; kk < p.last_ksteps; ++kk) {
+                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h) {
-                        const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
-                        umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                for (int h = 0; h < C::kHalves; ++h) {
+                    const uint64_t bd = smem_desc_sw128(b0 + 16384 * h + kk * 2048, 8192, 1024);
+                    umma_bf16_pair(d_tmem + 256u * h, ad, bd, idesc, (kfull | kk) != 0 ? 1u : 0u);
                 }
             }
             umma_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
@@ -1676,13 +1695,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_relinquish_pair();
     }
     build_expert_table(p.offsets, p.E, kTileM, mt_base, ctl->wsum);  // contain __syncthreads
-    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum);
+    build_expert_table(p.offsets, p.E, kRowsPerChunk, unit_base, ctl->wsum, p.nch);
     build_expert_table(p.offsets, p.E, 2 * kTileM, pt_base, ctl->wsum);
     if (mt_base[p.E] > p.max_mtiles || __ldg(p.offsets + p.E) != p.T * p.k) {
         __syncthreads();
         if (tid == 0) {
             report_error(p.status, kStDevice, -2, __ldg(p.offsets + p.E), 0);
-            for (int e = 0; e <= p.E; ++e) mt_base[e] = unit_base[e] = pt_base[e] = 0;
+            for (int e = 0; e <= p.E; ++e) mt_base[e] = pt_base[e] = 0;
+            for (int i = 0; i <= p.nch * p.E; ++i) unit_base[i] = 0;
         }
         __syncthreads();
     }
@@ -1721,7 +1741,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     if (warp == 0) {
-        if (lane == 0) pair_tma_role<STAGES, BN>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
+        if (lane == 0) {
+            if (p.gather) pair_tma_role<STAGES, BN, true>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
+            else pair_tma_role<STAGES, BN, false>(p, ctl, mt_base, pt_base, sA, sB, w, leader, peer);
+        }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && leader) pair_mma_role<STAGES, BN>(p, ctl, sA, sB, tmem_base, w);

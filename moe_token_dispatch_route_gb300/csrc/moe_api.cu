@@ -28,6 +28,7 @@ struct moe_plan_s {
     long long timeout_ns = 0;
     int skip_publish = -1;
     int band = 0;
+    int scatter_parts = 1;  // scatter order: parts per expert (chunk-major), nch E <= kMaxE
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
     bool single_ready = false;  // automatic pair plans: single-CTA kernel attributes set (direct gather)
     unsigned long long* trace = nullptr;  // per-CTA trace records (moe_set_trace), or null
@@ -238,6 +239,11 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->skip_publish = shape->debug_skip_publish > 0 ? shape->debug_skip_publish - 1 : -1;
     // tuning override for sweeps only: row tiles per schedule band (0 = whole expert)
     if (const char* env = std::getenv("MOE_TILE_BAND")) p->band = std::max(0, std::atoi(env));
+    // The scatter walks each expert's rows in token-ordered parts of about 1024 tokens (at
+    // most 16), part-major, so that a token's k copies are made while its x row is in L2.
+    p->scatter_parts = std::max(1, std::min(std::min(16, kMaxE / p->E), p->T / 1024));
+    if (const char* env = std::getenv("MOE_SCATTER_PARTS"))  // tuning override for sweeps only
+        p->scatter_parts = std::max(1, std::min(std::atoi(env), kMaxE / p->E));
 
     size_t off = kHdrBytes;
     p->ws.route_blk_off = off;
@@ -448,6 +454,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
+    prm.nch = plan->scatter_parts;
     cudaError_t lerr;
     if (gather && plan->pair && plan->shape.tile_m != 256) {
         // The direct gather of an automatic pair plan runs in the single-CTA kernel with

@@ -228,10 +228,10 @@ def test_pair_mode_last_tile_of_at_most_128_rows(T, tile_n):
     (1500, 4, 2, 1408),   # six column tiles, the last 128 wide
 ])
 def test_pair_mode_narrow_last_column_tile(T, E, k, N):
-    """256-wide pair tiles whose last column tile holds at most 128 columns run it as an
-    N=128 pair MMA, one 64-column B box per CTA.  Against the oracle, and (where 512-wide
-    tiles exist, N >= 512) bit for bit against 512-wide tiles, which issue N=256 MMAs
-    only: each element sees the same K order."""
+    """256-wide pair tiles whose last column tile holds at most 128 columns (its B boxes
+    partly or wholly outside W, zero-filled).  Against the oracle, and (where 512-wide
+    tiles exist, N >= 512) bit for bit against 512-wide tiles: each element sees the same
+    K order."""
     wl = workloads.custom("narrow", T, 128, E, k, N, 1, "none")
     plan, bufs = _full_check(wl, tile_m=256, tile_n=256)
     assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
