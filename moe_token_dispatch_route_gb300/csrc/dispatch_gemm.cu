@@ -786,6 +786,10 @@ struct Cfg {
 // the current tile, so the claim and flag latencies overlap the loads still
 // buffered ahead of the MMA.
 constexpr int kLookaheadKb = 4;
+// CTA pairs claim earlier, at k-block kPairClaimKb of the current tile: their TMA
+// thread is busy issuing for most of a tile, and a claim at the end of a short tile
+// (d = 2048: 32 k-blocks) stalls its issue while the ring is least full.
+constexpr int kPairClaimKb = 2;
 
 template <int BN, int STAGES>
 __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* mt_base,
@@ -1369,6 +1373,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     using C = PairCfg<STAGES, BN>;
     const uint32_t total_tiles = (uint32_t)pt_base[p.E] * (uint32_t)p.n_tiles;
     tma_prefetch_map(&p.b_map);
+    if (p.b3d) tma_prefetch_map(&p.b3_map);
     if (!GATHER)  // no A tensor map in the gather mode
         for (int r = 0; r < p.R; ++r) tma_prefetch_map(&p.a_map[r]);
     const uint32_t lead = leader ? cluster_ctarank() : peer;  // rank of the leader CTA
@@ -1457,7 +1462,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
             for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, cur.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
-        const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
+        const int pre_kb = p.k_blocks > kPairClaimKb ? kPairClaimKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
         bool have_next = false;
@@ -1481,10 +1486,17 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
                 tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             }
+            if (p.b3d) {  // boxes 2h and 2h + 1 are adjacent chunks: one copy each h
 #pragma unroll
-            for (int b = 0; b < 2 * C::kHalves; ++b)
-                tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
-                                 brow + kb * kTileK);
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d_pair(smem_addr(sB + stage * C::kBBytes + 16384 * h), &p.b3_map, fb, 0,
+                                     brow + kb * kTileK, bcol[2 * h] >> 6);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 2 * C::kHalves; ++b)
+                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                     brow + kb * kTileK);
+            }
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;

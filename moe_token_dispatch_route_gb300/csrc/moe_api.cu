@@ -41,6 +41,8 @@ struct moe_plan_s {
     const void* map_A[kMaxRanks] = {};
     CUtensorMap a_maps[kMaxRanks];
     CUtensorMap b_map;
+    CUtensorMap b3_map;  // W as 64-column chunks (valid when b3_ok)
+    bool b3_ok;
 };
 
 namespace {
@@ -93,6 +95,22 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// W [rows][cols] bf16 (cols % 64 == 0) as 64-column chunks: dims {64, rows, cols/64}
+// with strides {cols*2, 128} bytes, box 64 x 64 x 2, 128-byte swizzle: one copy moves
+// two adjacent chunks, landing exactly as two boxes of the 2-D map one after the other.
+bool encode_bf16_chunks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+    auto enc = tensor_map_encoder();
+    if (!enc || cols % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -403,6 +421,8 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
             if (!encode_bf16_2d(&plan->b_map, W, (uint64_t)plan->E * plan->d, (uint64_t)plan->N, 64,
                                 kTileK))
                 return MOE_ERR_CUDA;
+            // the chunked view is an optimisation: where it cannot be encoded the 2-D map serves
+            plan->b3_ok = encode_bf16_chunks(&plan->b3_map, W, (uint64_t)plan->E * plan->d, (uint64_t)plan->N);
             plan->map_W = W;
             plan->map_nA = nA;
             plan->map_rows = arows;
@@ -412,6 +432,10 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
         std::memset(&prm, 0, sizeof prm);
         for (int r = 0; r < nA; ++r) prm.a_map[r] = plan->a_maps[r];
         prm.b_map = plan->b_map;
+        prm.b3_map = plan->b3_map;
+        // chunk pairs must start on a chunk boundary: N % 64 == 0, and F % 64 == 0 for the
+        // gated layout (its up half starts at column F)
+        prm.b3d = (plan->b3_ok && (!glu || (plan->N / 2) % 64 == 0)) ? 1 : 0;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.x = x;

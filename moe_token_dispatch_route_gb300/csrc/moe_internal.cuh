@@ -81,6 +81,8 @@ cudaError_t route_prepare_attributes();
 struct DispatchGemmParams {
     CUtensorMap a_map[kMaxRanks];   // rank receive buffers, bf16 [cap][d], box 64 x 128
     CUtensorMap b_map;              // W viewed as bf16 [E*d][N], box 64 x 64
+    CUtensorMap b3_map;             // W as 64-column chunks: dims {64, E*d, N/64}, box 64 x 64 x 2
+    int b3d;                        // 1: B boxes are loaded two chunks at a time through b3_map
     const uint16_t* x;
     const int32_t* offsets;
     const int32_t* perm;
@@ -404,6 +406,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // TMA tile load whose completion is signalled on an mbarrier of either CTA of the pair
+// Two adjacent 64-column chunks of W in one copy (3-D map {64, rows, chunks}, box
+// 64 x 64 x 2): they land as two 8 KB 128-byte-swizzled boxes, one after the other.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
                                                  int c0, int c1) {
     asm volatile(
