@@ -122,6 +122,11 @@ typedef struct moe_plan_info {
     int32_t max_mtiles;               /* upper bound on 128-row tiles: floor(S/128) + E */
     int32_t route_blocks;             /* CTAs of the routing kernel                     */
     int64_t workspace_bytes;          /* size moe_plan reported                         */
+    int32_t half_tiles;               /* 1: a moe_dispatch_gemm / moe_grouped_gemm /
+                                         moe_gather_gemm schedule of at most num_ctas/2
+                                         tiles runs each tile as two half-width tiles
+                                         (the same bits; single-CTA plans of tile_n 128
+                                         or 256); 0: whole tiles only                   */
 } moe_plan_info_t;
 
 /*
@@ -326,7 +331,8 @@ MOE_API moe_status_t moe_grouped_gemm(moe_plan_t plan, const uint16_t* A, const 
  *                  tracing off (the default).  Each launch overwrites record b
  *                  (words 8b .. 8b+7) of every CTA b it runs:
  *                  0 start, 1 end of its scatter share (0 if none), 2 first
- *                  tile's rows ready, 4 tiles it loaded, 5 last load issued,
+ *                  tile's rows ready, 4 tiles it loaded (the halves of a split
+ *                  tile count as two), 5 last load issued,
  *                  6 end (global-timer ns); 3 total ns waiting for ready flags;
  *                  7 its role ticket.
  * The records cost a few stores per tile.  Host only; no launch.

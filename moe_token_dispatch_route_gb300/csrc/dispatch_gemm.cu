@@ -59,6 +59,8 @@ struct TileInfo {
     int arow;  // first row inside the rank's receive buffer
     int m128;  // CTA pairs: 1 for an expert's last tile of at most 128 rows, run as an
                // M=128 pair MMA (64 rows per CTA); 0 otherwise
+    int half;  // single CTAs: 0 the whole tile; 1 / 2 its left / right half of the columns
+               // (small schedules run every tile as two halves)
 };
 
 constexpr int kMaxPieceBufs = 8;
@@ -634,6 +636,9 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
                                               uint32_t tbase, int q, int lane, float* epi,
                                               const CombineRow& cr) {
     const int rows_valid = min(32, ti.rows - 32 * q);  // rows of this warp's lane quarter
+    // output columns of the tile (TMEM columns from 0): the whole tile or one half
+    const int cw = ti.half ? bn / 2 : bn;
+    const int c0 = ti.n * bn + (ti.half ? (ti.half - 1) * cw : 0);
     if (p.glu) {
         const int half = bn / 2;
         const int fcols = min(half, p.F - ti.n * half);
@@ -657,8 +662,8 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
                                  (fcols - c) / 2, lane);
         }
     } else if (p.out_bf16) {
-        uint16_t* ybase = static_cast<uint16_t*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
-        const int ncols = min(bn, p.N - ti.n * bn);
+        uint16_t* ybase = static_cast<uint16_t*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)c0;
+        const int ncols = min(cw, p.N - c0);
         for (int c = 0; c < ncols; c += 64) {
             uint32_t w[32];
 #pragma unroll
@@ -684,8 +689,8 @@ __device__ __forceinline__ void epilogue_tile(const DispatchGemmParams& p, const
                 red_block_rows(epi, v, p.out, (size_t)p.N, ti.n * bn + c, rows_valid, ncols - c, lane, cr);
         }
     } else {
-        float* ybase = static_cast<float*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)ti.n * bn;
-        const int ncols = min(bn, p.N - ti.n * bn);
+        float* ybase = static_cast<float*>(p.Y) + (size_t)(ti.row0 + 32 * q) * p.N + (size_t)c0;
+        const int ncols = min(cw, p.N - c0);
         for (int c = 0; c < ncols; c += 32) {
             uint32_t v[32];
             tmem_ld_32x32(tbase + (uint32_t)c, v);
@@ -768,6 +773,7 @@ struct Cfg {
     static constexpr int kBBytes = BN * kTileK * 2;      // BN/64 boxes of 64 x 64
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kIdesc = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN);
+    static constexpr uint32_t kIdescHalf = idesc_bf16_f32_kmajA_mnmajB(kTileM, BN / 2);  // split tiles
     static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;  // allocations are powers of two
     static constexpr size_t kSmem =
         1024 + (size_t)STAGES * kStageBytes + kEpiBytes + sizeof(SmemCtl) + 2 * sizeof(int) * (kMaxE + 1);
@@ -796,6 +802,12 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
                          uint8_t* sA, uint8_t* sB, const Waiter& w) {
     using C = Cfg<BN, STAGES>;
     const uint32_t total_tiles = (uint32_t)mt_base[p.E] * (uint32_t)p.n_tiles;
+    // claims below split_from are whole tiles; each tile from split_from on is claimed twice,
+    // as its left and its right half: every tile of a schedule that fills at most half the
+    // grid (half_tiles 1), or always (2)
+    const bool split = p.half_tiles == 2 || (p.half_tiles == 1 && 2u * total_tiles <= gridDim.x);
+    const uint32_t split_from = split ? 0u : total_tiles;
+    const uint32_t total_claims = 2u * total_tiles - split_from;
     const int e_per_rank = p.E / p.R;
     tma_prefetch_map(&p.b_map);
     if (!p.gather)  // no A tensor map in the gather mode
@@ -811,11 +823,13 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     // claim a tile, describe it, hand it to the MMA and epilogue warps, read its flag
     auto push_next = [&](TileInfo& ti, uint32_t& flag) -> bool {
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
-        const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
-        if (tile >= total_tiles) {
-            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = 0;
+        const uint32_t claim = atomicAdd(p.hdr + kHdrTileCtr, 1u);
+        if (claim >= total_claims) {
+            ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = ti.half = 0;
             ti.rows = -1;
         } else {
+            const uint32_t tile = claim < split_from ? claim : split_from + (claim - split_from) / 2;
+            ti.half = claim < split_from ? 0 : 1 + (int)((claim - split_from) & 1u);
             const int u = (int)(tile / (uint32_t)p.n_tiles);
             const int e = expert_of(mt_base, p.E, u);
             const int mt_e = mt_base[e + 1] - mt_base[e];
@@ -868,6 +882,11 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         fence_proxy_async_global();
         const CUtensorMap* amap = &p.a_map[cur.rank];
         const int brow = cur.e * p.d;
+        // B boxes of the tile: all BN/64, or the BN/128 of one half (split tiles are never
+        // gated, so a half's boxes are consecutive columns)
+        const int nbox = cur.half ? BN / 128 : BN / 64;
+        const int bshift = cur.half == 2 ? BN / 2 : 0;
+        const uint32_t b_bytes = (uint32_t)nbox * 8192u;
         const int pre_kb = p.k_blocks > kLookaheadKb ? p.k_blocks - kLookaheadKb : 0;
         TileInfo nxt;
         uint32_t nxt_flag = 0;
@@ -882,15 +901,16 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
             }
             const uint32_t fb = smem_addr(&ctl->full[stage]);
             if (p.gather) {  // the gather warps fill A and arrive on the same barrier
-                mbar_arrive_expect_tx(fb, C::kBBytes);
+                mbar_arrive_expect_tx(fb, b_bytes);
             } else {
-                mbar_arrive_expect_tx(fb, C::kStageBytes);
+                mbar_arrive_expect_tx(fb, C::kABytes + b_bytes);
                 tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             }
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
-                            b_box_col(p, cur.n, BN, j), brow + kb * kTileK);
+                if (j < nbox)
+                    tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
+                                b_box_col(p, cur.n, BN, j) + bshift, brow + kb * kTileK);
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -921,6 +941,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
     while (ok) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 4)) break;
         const int rows = ctl->ring[slot].rows;
+        const uint32_t idesc = ctl->ring[slot].half ? C::kIdescHalf : C::kIdesc;  // N = BN or BN/2
         mbar_arrive(smem_addr(&ctl->sempty[slot]));
         if (++slot == kRing) {
             slot = 0;
@@ -950,7 +971,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
                 //    1024 B apart (SBO); K step of 16 rows = +2048 B.
                 const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                 const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             }
             umma_commit(smem_addr(&ctl->empty[stage]));
             if (++stage == STAGES) {
@@ -966,7 +987,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
             for (int kk = 0; kk < p.last_ksteps; ++kk) {
                 const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                 const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
-                umma_bf16(d_tmem, ad, bd, C::kIdesc, (kfull | kk) != 0 ? 1u : 0u);
+                umma_bf16(d_tmem, ad, bd, idesc, (kfull | kk) != 0 ? 1u : 0u);
             }
             umma_commit(smem_addr(&ctl->empty[stage]));
             if (++stage == STAGES) {
@@ -1349,6 +1370,7 @@ __device__ void pair_half_info(const DispatchGemmParams& p, const int* mt_base, 
     const int cnt = __ldg(p.offsets + e + 1) - seg0;
     ti.e = e;
     ti.n = n;
+    ti.half = 0;
     ti.m128 = (!p.glu && cnt - 2 * kTileM * m2 <= kTileM) ? 1 : 0;
     if (ti.m128) {
         ti.m = 2 * m2;
@@ -1396,7 +1418,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             const uint32_t tile = atomicAdd(p.hdr + kHdrTileCtr, 1u);
             TileInfo other;
             if (tile >= total_tiles) {
-                ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = 0;
+                ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rows = ti.rank = ti.arow = ti.m128 = ti.half = 0;
                 ti.e = -1;
                 other = ti;
             } else {

@@ -28,6 +28,7 @@ struct moe_plan_s {
     long long timeout_ns = 0;
     int skip_publish = -1;
     int band = 0;
+    int half_tiles = 0;  // single-CTA plans: 1 = small schedules run as half-width tiles
     int scatter_parts = 1;  // scatter order: parts per expert (chunk-major), nch E <= kMaxE
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
     bool single_ready = false;  // automatic pair plans: single-CTA kernel attributes set (direct gather)
@@ -257,6 +258,14 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     p->skip_publish = shape->debug_skip_publish > 0 ? shape->debug_skip_publish - 1 : -1;
     // tuning override for sweeps only: row tiles per schedule band (0 = whole expert)
     if (const char* env = std::getenv("MOE_TILE_BAND")) p->band = std::max(0, std::atoi(env));
+    // A schedule with fewer tiles than half the CTAs (a small, latency-bound layer) leaves
+    // most SMs idle; there every single-CTA tile is claimed as two half-width tiles, left
+    // and right, which the kernel decides once routing has fixed the tile count.  Halves
+    // need whole 64-column boxes: BN 128 or 256.  (Splitting the last wave of a large
+    // HBM-bound layer instead was measured slower: a half carries the whole A traffic.)
+    if (!p->pair && (p->tile_n == 128 || p->tile_n == 256)) p->half_tiles = 1;
+    if (const char* env = std::getenv("MOE_HALF_TILES"))  // tuning override: 0 never, 2 always
+        p->half_tiles = p->half_tiles ? std::max(0, std::min(2, std::atoi(env))) : 0;
     // The scatter walks each expert's rows in token-ordered parts of about 1024 tokens (at
     // most 16), part-major, so that a token's k copies are made while its x row is in L2.
     p->scatter_parts = std::max(1, std::min(std::min(16, kMaxE / p->E), p->T / 1024));
@@ -303,6 +312,7 @@ moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info) {
     info->max_mtiles = plan->max_mtiles;
     info->route_blocks = plan->route_blocks;
     info->workspace_bytes = (int64_t)plan->ws.total;
+    info->half_tiles = plan->half_tiles;
     return MOE_OK;
 }
 
@@ -478,6 +488,8 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.max_mtiles = plan->max_mtiles;
     prm.skip_publish = plan->skip_publish;
     prm.band = plan->band;
+    // gated and combining epilogues keep whole tiles (their column bookkeeping is per tile)
+    prm.half_tiles = (glu || combine) ? 0 : plan->half_tiles;
     prm.nch = plan->scatter_parts;
     cudaError_t lerr;
     if (gather && plan->pair && plan->shape.tile_m != 256) {

@@ -100,6 +100,8 @@ struct DispatchGemmParams {
     int max_mtiles;                 // size of flags[] and chunk_cnt[]
     int skip_publish;               // m-tile whose flag is never published, or -1
     int band;                       // row tiles per schedule band; 0 = the whole expert
+    int half_tiles;                 // single CTAs: 0 whole tiles only; 1 every tile as two half-width
+                                    //   tiles when the schedule has at most gridDim/2 tiles; 2 always
     int nch;                        // scatter order: parts per expert, chunk-major (nch E <= 1024)
     int glu;                        // 1: W = [gate | up], each F = N/2 wide; out H, not Y
     int F;                          // N/2 when glu

@@ -93,6 +93,44 @@ def test_role_split_and_grid_do_not_change_bits():
         assert torch.equal(outs[0], o)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_half_width_tiles_do_not_change_bits(tile_n, monkeypatch):
+    """Single-CTA tiles claimed as left and right halves (N = BN/2 MMAs): whole tiles,
+    the default (halves only for small schedules) and every tile split give the same
+    bits, for fp32 and bf16 Y and for the direct gather; the split run against the oracle."""
+    wl = workloads.custom("tsplit", 700, 256, 8, 2, 656, 2, "zipf")  # ragged last column tile
+    inp = workloads.make_inputs(wl, seed=30)
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+    Yref = oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"])
+    x, W = inp["x"].cuda(), inp["W"].cuda()
+    for out_dtype in (binding.MOE_OUT_F32, binding.MOE_OUT_BF16):
+        bf16 = out_dtype == binding.MOE_OUT_BF16
+        outs = []
+        for split in ("0", None, "2"):
+            if split is None:
+                monkeypatch.delenv("MOE_HALF_TILES", raising=False)
+            else:
+                monkeypatch.setenv("MOE_HALF_TILES", split)
+            plan, bufs, rc, status = run_path(wl, inp, tile_m=128, tile_n=tile_n, out_dtype=out_dtype)
+            assert rc == 0, status
+            assert plan.info["half_tiles"] == (0 if split == "0" else 2 if split == "2" else 1)
+            outs.append(bufs.Y.clone())
+            if not bf16:
+                bufs.Y.fill_(float("nan"))
+                binding.gather_gemm(plan, x, W, bufs)
+                rc, status = binding.moe_read_status(bufs.status)
+                assert rc == 0, status
+                assert torch.equal(outs[-1], bufs.Y)
+        for o in outs[1:]:
+            assert torch.equal(outs[0].view(torch.int16 if bf16 else torch.int32),
+                               o.view(torch.int16 if bf16 else torch.int32))
+        if bf16:
+            _check_bf16(outs[2].float().cpu().double().numpy(), Yref)
+        else:
+            check_Y(outs[2].cpu().double().numpy(), Yref)
+
+
 def test_repeated_calls_reuse_workspace():
     """Epoch-tagged flags: back-to-back calls on one workspace, outputs poisoned
     between calls, every call complete and identical."""
