@@ -13,7 +13,9 @@ namespace moe {
 
 constexpr int kRouteChunk = 64;     // most tokens per routing CTA (8..64, a power of two)
 constexpr int kRouteFuseSlots = 8192;  // T*k up to this: the last routing CTA also permutes
-constexpr int kRouteThreads = 256;  // 8 warps
+// threads of a routing CTA: 8 warps for E <= 32, 16 for more experts (measured: 16 warps
+// route the E = 64 and 256 batches 14-18% faster and the E = 8 ones 7-12% slower)
+constexpr int route_threads(int E) { return E <= 32 ? 256 : 512; }
 
 constexpr int kTileM = 128;         // GEMM rows per tile (one UMMA M=128)
 constexpr int kTileK = 64;          // bf16 elements per 128-byte swizzle row

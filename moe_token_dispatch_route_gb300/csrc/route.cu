@@ -9,8 +9,8 @@
 // and a destination order grouped by expert, then token, then slot.
 //
 // Two launches, no atomics that decide an order:
-//  1. route_select_kernel: one CTA per 8-64 tokens, one warp per token at a
-//     time.  Each warp holds its token's E logits in registers (E/32 per
+//  1. route_select_kernel: one CTA per 8-64 tokens (8 warps, or 16 when
+//     E > 32), one warp per token at a time.  Each warp holds its token's E logits in registers (E/32 per
 //     lane), takes their maximum with a warp max over order-preserving
 //     integer keys and their sum of exponentials with xor shuffles, and runs
 //     k rounds of a warp arg-max (a warp max of the keys, then a warp min of
@@ -31,10 +31,10 @@
 namespace moe {
 namespace {
 
-template <int VPL>  // logits per lane: E <= 32 * VPL
-__global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const RouteArgs a) {
+template <int VPL, int NT>  // logits per lane: E <= 32 * VPL; NT threads
+__global__ void __launch_bounds__(NT) route_select_kernel(const RouteArgs a) {
     extern __shared__ uint32_t smem[];
-    select_chunk<VPL>(a, blockIdx.x, smem);
+    select_chunk<VPL, NT>(a, blockIdx.x, smem);
     const int tid = threadIdx.x, E = a.E;
     const int chunk = a.chunk;
 
@@ -46,13 +46,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(const Route
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    __shared__ int part[kMaxE], tot[kMaxE], wsum[kRouteThreads / 32];
-    scan_counts(a, part, tot, wsum);
+    __shared__ int part[kMaxE], tot[kMaxE], wsum[NT / 32];
+    scan_counts<NT>(a, part, tot, wsum);
     if (a.fuse_permute) {
         // small batches: this CTA also turns every slot's rank into its destination row
         __syncthreads();
         const int S = a.T * a.k;
-        for (int s = tid; s < S; s += kRouteThreads) {
+        for (int s = tid; s < S; s += NT) {
             const int b = (s / a.k) / chunk;
             const int e = __ldcg(a.topk_idx + s);
             if (e < 0 || e >= E) continue;
@@ -81,7 +81,8 @@ size_t select_smem_bytes(int E, int k) { return select_smem_words(E, k) * 4; }
 
 template <int VPL>
 cudaError_t launch_select(const RouteArgs& a, cudaStream_t stream) {
-    route_select_kernel<VPL><<<a.nb, kRouteThreads, select_smem_bytes(a.E, a.k), stream>>>(a);
+    constexpr int NT = route_threads(32 * VPL);  // the same for every E of this VPL
+    route_select_kernel<VPL, NT><<<a.nb, NT, select_smem_bytes(a.E, a.k), stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -26,8 +26,10 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Exclusive scan of n <= 1024 ints held in smem `vals`, in place, by 256 threads;
-// returns the total to every thread.  `wsum` is 8 ints of scratch.
+// Exclusive scan of n <= 1024 ints held in smem `vals`, in place, by NT >= 256
+// threads (four values each); returns the total to every thread.  `wsum` is NT/32
+// ints of scratch.
+template <int NT>
 __device__ int block_exclusive_scan_1024(int* vals, int n, int* wsum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int base = tid * 4;
@@ -48,7 +50,7 @@ __device__ int block_exclusive_scan_1024(int* vals, int n, int* wsum) {
     __syncthreads();
     int pre = 0, total = 0;
 #pragma unroll
-    for (int w = 0; w < kRouteThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         if (w < warp) pre += wsum[w];
         total += wsum[w];
     }
@@ -64,13 +66,14 @@ __device__ int block_exclusive_scan_1024(int* vals, int n, int* wsum) {
 
 // Runs in the last routing CTA: per-CTA counts blk[b][e] -> counts, offsets and
 // per-CTA bases blk[b][e] = offsets[e] + sum_{b' < b} count[b'][e].  Shared-memory
-// scratch: part and tot of kMaxE ints each, wsum of kRouteThreads / 32 ints.
+// scratch: part and tot of kMaxE ints each, wsum of NT / 32 ints.
+template <int NT>
 __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) {
     const int tid = threadIdx.x;
     const int E = a.E, nb = a.nb;
-    const int G = E >= kRouteThreads ? 1 : kRouteThreads / E;  // CTA groups per expert
+    const int G = E >= NT ? 1 : NT / E;  // CTA groups per expert
     // 1. partial sums over contiguous CTA ranges
-    for (int job = tid; job < G * E; job += kRouteThreads) {
+    for (int job = tid; job < G * E; job += NT) {
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int s = 0;
@@ -85,7 +88,7 @@ __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) 
     }
     __syncthreads();
     // 2. per expert: exclusive prefix over the groups, and the total
-    for (int e = tid; e < E; e += kRouteThreads) {
+    for (int e = tid; e < E; e += NT) {
         int run = 0;
         for (int g = 0; g < G; ++g) {
             const int c = part[g * E + e];
@@ -95,14 +98,14 @@ __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) 
         tot[e] = run;
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kRouteThreads) a.counts[e] = tot[e];
+    for (int e = tid; e < E; e += NT) a.counts[e] = tot[e];
     __syncthreads();
     // 3. exclusive scan over experts -> offsets
-    const int total = block_exclusive_scan_1024(tot, E, wsum);
-    for (int e = tid; e < E; e += kRouteThreads) a.offsets[e] = tot[e];
+    const int total = block_exclusive_scan_1024<NT>(tot, E, wsum);
+    for (int e = tid; e < E; e += NT) a.offsets[e] = tot[e];
     if (tid == 0) a.offsets[E] = total;
     // 4. per-CTA bases, written over the per-CTA counts
-    for (int job = tid; job < G * E; job += kRouteThreads) {
+    for (int job = tid; job < G * E; job += NT) {
         const int e = job % E, g = job / E;
         const int b0 = (int)((long long)nb * g / G), b1 = (int)((long long)nb * (g + 1) / G);
         int run = tot[e] + part[job];
@@ -121,23 +124,23 @@ __device__ void scan_counts(const RouteArgs& a, int* part, int* tot, int* wsum) 
 }
 
 
-// Routing chunk c (tokens [c * chunk, (c + 1) * chunk)) by the calling CTA's 256
+// Routing chunk c (tokens [c * chunk, (c + 1) * chunk)) by the calling CTA's NT
 // threads: top-k and gates per token (one warp per token at a time), then the
 // chunk's per-expert counts into blk[c][*] and every slot's rank among the chunk's
 // rows of its expert into dest.  `smem`: E * kMaskWords + kRouteChunk * k words.
-template <int VPL>  // logits per lane: E <= 32 * VPL
+template <int VPL, int NT>  // logits per lane: E <= 32 * VPL; NT threads
 __device__ void select_chunk(const RouteArgs& a, int c, uint32_t* smem) {
     const int E = a.E, k = a.k;
     uint32_t* mask = smem;                                              // [E][kMaskWords]
     int32_t* sel = reinterpret_cast<int32_t*>(mask + E * kMaskWords);  // [kRouteChunk][k]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < E * kMaskWords; i += kRouteThreads) mask[i] = 0u;
+    for (int i = tid; i < E * kMaskWords; i += NT) mask[i] = 0u;
     __syncthreads();
 
     const int chunk = a.chunk;
     const int t0 = c * chunk;
     const int ntok = min(chunk, a.T - t0);
-    for (int tl = warp; tl < ntok; tl += kRouteThreads / 32) {
+    for (int tl = warp; tl < ntok; tl += NT / 32) {
         const int t = t0 + tl;
         const float* L = a.logits + (size_t)t * E;
         float v[VPL];
@@ -221,13 +224,13 @@ __device__ void select_chunk(const RouteArgs& a, int c, uint32_t* smem) {
 
     // per-CTA counts and each slot's rank among this CTA's rows of its expert
     int32_t* blk = a.blk + (size_t)c * E;
-    for (int e = tid; e < E; e += kRouteThreads) {
+    for (int e = tid; e < E; e += NT) {
         int c = 0;
 #pragma unroll
         for (int w = 0; w < kMaskWords; ++w) c += __popc(mask[e * kMaskWords + w]);
         blk[e] = c;
     }
-    for (int q = tid; q < ntok * k; q += kRouteThreads) {
+    for (int q = tid; q < ntok * k; q += NT) {
         const int tl = q / k;
         const int e = sel[q];
         if (e < 0 || e >= E) continue;
