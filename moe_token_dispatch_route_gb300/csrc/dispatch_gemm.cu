@@ -803,8 +803,8 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     using C = Cfg<BN, STAGES>;
     const uint32_t total_tiles = (uint32_t)mt_base[p.E] * (uint32_t)p.n_tiles;
     // claims below split_from are whole tiles; each tile from split_from on is claimed twice,
-    // as its left and its right half: every tile of a schedule that fills at most half the
-    // grid (half_tiles 1), or always (2)
+    // as its left and its right half.  split_from is 0 (every tile split) when the schedule
+    // fills at most half the grid (half_tiles 1) or always (half_tiles 2), else total_tiles.
     const bool split = p.half_tiles == 2 || (p.half_tiles == 1 && 2u * total_tiles <= gridDim.x);
     const uint32_t split_from = split ? 0u : total_tiles;
     const uint32_t total_claims = 2u * total_tiles - split_from;
