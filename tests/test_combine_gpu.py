@@ -141,17 +141,19 @@ def test_fused_combine_is_bitwise_repeatable_across_role_splits_and_grids(k):
             assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
 
 
-def test_fused_combine_mixtral_full_size_sampled():
-    """The Mixtral-shaped layer in the benchmark's launch configuration: every output
-    element written (poisoned first), and sampled tokens whose slots fall in every
-    (row tile, column tile) of the GEMM against the oracle's combine."""
-    wl = workloads.WORKLOADS["mixtral"]
+@pytest.mark.parametrize("name", ["mixtral", "finegrained", "deepseek_v3", "decode"])
+def test_fused_combine_full_size_sampled(name):
+    """Each large layer in the benchmark's launch configuration (k = 2, 4, 8, 8): every
+    output element written (poisoned first), and sampled tokens whose slots fall in every
+    (row tile, column tile) of the GEMM, with all k terms, against the oracle's combine."""
+    wl = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(wl, seed=0, w_device="cuda")
     plan, bufs, out, rc, st = _fused(wl, inp)
     assert rc == 0, st
     assert not torch.isnan(out).any().item(), "unwritten output"
     ref = oracle.route(inp["logits"].numpy(), wl.k)
-    rows, cols = sample_rows_cols(ref, wl.N, tile_n=plan.info["tile_n"], n_random=16)
+    rows, cols = sample_rows_cols(ref, wl.N, tile_m=plan.info["tile_m"], tile_n=plan.info["tile_n"],
+                                  n_random=16)
     toks = sorted({int(ref["perm"][r]) // wl.k for r in rows})
     # both slots of every sampled token, as destination rows, and the oracle's Y there
     slots = np.array([t * wl.k + j for t in toks for j in range(wl.k)])
