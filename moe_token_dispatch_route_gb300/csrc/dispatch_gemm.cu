@@ -927,7 +927,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
         if (last_phase[s] >= 0) wait_bar(smem_addr(&ctl->full[s]), (uint32_t)last_phase[s], w, 3, false);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool GATHER>
 __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, uint8_t* sB,
                          uint32_t tmem_base, const Waiter& w) {
     using C = Cfg<BN, STAGES>;
@@ -961,6 +961,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
                 ok = false;
                 break;
             }
+            if (GATHER) fence_proxy_async_smem();  // the gather threads' rows
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
@@ -981,6 +982,7 @@ __device__ void mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA,
         }
         if (ok && kfull < p.k_blocks) {  // the short last k-block
             if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 6)) break;
+            if (GATHER) fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
@@ -1051,18 +1053,17 @@ __device__ void epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, uint32_
 // 128-byte-swizzled K-major layout the MMA descriptors expect (16-byte chunk c of
 // row r lands at r*128 + (c ^ (r%8))*16).  Eight lanes cover one row's 128 bytes of
 // a k-block, so each copy instruction moves four whole 128-byte lines.  Rows past
-// the tile's valid rows are zero-filled.  Each warp keeps up to STAGES-2 stages of
-// copies in flight; once a stage's copies are complete it fences them for the async
-// proxy (the tensor cores read shared memory there) and arrives on the stage's full
-// barrier, which also waits for the other gather warps and the B bytes.  In CTA
-// pairs that is the leader's barrier: the peer's warps arrive on it remotely
-// (release at cluster scope), since the leader's MMAs read both CTAs' rows.  No
-// receive buffer is written and no ready flag is read.  In CTA pairs the peer's
-// gather warps arrive on the peer's own `afull` barrier, and the peer's relay thread
-// (pair_relay_role) passes each completed stage on to the leader's stage barrier.
-// The copies are cp.async by warps, not TMA: a TMA gather of four 128-byte rows
-// (tile::gather4) per lane ran about 3x slower than this here (32 small TMA
-// operations per k-block and CTA).
+// the tile's valid rows are zero-filled.  Every thread ends a stage's copies with a
+// cp.async-completion arrival (.noinc) on the stage's barrier, so a stage is
+// published as soon as its rows have landed and the warps never wait for their own
+// copies: on the full barrier (with the B bytes) in single CTAs and the pair leader,
+// on the CTA's own `afull` barrier in the pair peer, whose relay thread
+// (pair_relay_role) passes each completed stage on to the leader.  The consumers
+// fence the copies for the async proxy (the tensor cores read shared memory there)
+// after their wait: the MMA thread for its CTA's rows, the relay for the peer's.  No
+// receive buffer is written and no ready flag is read.  The copies are cp.async by
+// warps, not TMA: a TMA gather of four 128-byte rows (tile::gather4) per lane ran
+// about 3x slower than this here (32 small TMA operations per k-block and CTA).
 constexpr int kGatherWarp0 = 2;
 constexpr int kGatherWarps = 2;
 constexpr int kGatherRows = kTileM / kGatherWarps;  // rows per warp
@@ -1070,7 +1071,6 @@ template <int STAGES>
 __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, const Waiter& w,
                               int part, bool pair, bool leader, uint32_t lead) {
     constexpr int kABytes = kTileM * kTileK * 2;  // 128 rows x 64 columns
-    constexpr int kLag = STAGES - 2 >= 1 ? STAGES - 2 : 1;  // stages in flight before an arrive
     constexpr int kIters = kGatherRows / 4;
     const int lane = threadIdx.x & 31;
     const char* xb = reinterpret_cast<const char*>(p.x);
@@ -1079,16 +1079,6 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
     uint32_t sphase = 0;
     int stage = 0;
     uint32_t phase = 0;
-    int pend[kMaxStages] = {};  // stages whose copies are in flight, oldest first
-    int head = 0, npend = 0;
-    auto retire_oldest = [&](int keep) {
-        cp_async_wait_dyn(keep);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(leader ? &ctl->full[pend[head]] : &ctl->afull[pend[head]]));
-        head = head + 1 == kMaxStages ? 0 : head + 1;
-        --npend;
-    };
     bool ok = true;
     while (ok) {
         const bool got = wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 40, true, pair);
@@ -1143,28 +1133,22 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
                 cp_async16_cg_zfill(a0 + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4),
                                     xb + (size_t)(t < 0 ? 0 : t) * row_bytes + kofs, (t < 0 || !in_row) ? 0 : 16);
             }
-            cp_async_commit();
-            int tail = head + npend;
-            if (tail >= kMaxStages) tail -= kMaxStages;
-            pend[tail] = stage;
-            ++npend;
-            if (npend > kLag) retire_oldest(kLag);
+            cp_async_mbar_arrive_noinc(smem_addr(leader ? &ctl->full[stage] : &ctl->afull[stage]));
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
     }
-    // every copy lands and is published before the CTA can leave (also on abort,
-    // so that the TMA thread's drain of the full barriers ends)
-    while (npend > 0) retire_oldest(0);
+    // no copy may still be landing when the CTA leaves (also after an abort)
+    cp_async_wait_all();
 }
 
 // Gather mode, peer CTA of a pair (its otherwise idle warp 1, lane 0): follows the
 // schedule ring and, for every stage, waits until the peer's gather warps have landed
 // their A rows (the peer's `afull` barrier) and then arrives on the leader's stage
-// barrier, which the leader's MMA thread waits on.  One cluster-scope arrival per
-// stage from this thread, instead of one from each gather warp.
+// barrier, which the leader's MMA thread waits on.  One remote arrival per stage
+// from this thread, instead of one from each gather thread.
 template <int STAGES>
 __device__ void pair_relay_role(const DispatchGemmParams& p, SmemCtl* ctl, const Waiter& w, uint32_t lead) {
     int stage = 0;
@@ -1181,8 +1165,10 @@ __device__ void pair_relay_role(const DispatchGemmParams& p, SmemCtl* ctl, const
         }
         if (e < 0) return;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!wait_bar(smem_addr(&ctl->afull[stage]), phase, w, 32, true, true)) return;
-            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->full[stage]), lead));
+            // afull's arrivals are this CTA's own copies: a CTA-scope wait
+            if (!wait_bar(smem_addr(&ctl->afull[stage]), phase, w, 32, true, false)) return;
+            fence_proxy_async_smem();  // the gathered rows, before the leader's MMAs read them
+            mbar_arrive_remote(mapa_shared(smem_addr(&ctl->full[stage]), lead));
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -1208,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + kGatherWarps : 1);  // + gather warps
+            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + 32 * kGatherWarps : 1);  // + gather threads
             mbar_init(smem_addr(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -1273,7 +1259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tma_role<BN, STAGES>(p, ctl, mt_base, sA, sB, w);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) mma_role<BN, STAGES>(p, ctl, sA, sB, tmem_base, w);
+        if (lane == 0) {
+            if (p.gather) mma_role<BN, STAGES, true>(p, ctl, sA, sB, tmem_base, w);
+            else mma_role<BN, STAGES, false>(p, ctl, sA, sB, tmem_base, w);
+        }
         __syncwarp();
     } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
         gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0, false, true, 0);
@@ -1541,7 +1530,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     }
 }
 
-template <int STAGES, int BN>
+template <int STAGES, int BN, bool GATHER>
 __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sA, uint8_t* sB,
                               uint32_t tmem_base, const Waiter& w) {
     using C = PairCfg<STAGES, BN>;
@@ -1575,6 +1564,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
                 ok = false;
                 break;
             }
+            if (GATHER) fence_proxy_async_smem();  // this CTA's gathered rows
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
@@ -1595,6 +1585,7 @@ __device__ void pair_mma_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         }
         if (ok && kfull < p.k_blocks) {  // the short last k-block
             if (!wait_bar(smem_addr(&ctl->full[stage]), phase, w, 27, true, true)) break;
+            if (GATHER) fence_proxy_async_smem();
             tc_fence_after();
             const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
             const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
@@ -1704,8 +1695,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             // leader: its expect_tx arrival + both CTAs' bytes (+ its gather warps and the
             // peer's relay in the gather mode); peer's afull: its gather warps
-            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + kGatherWarps + 1 : 1);
-            mbar_init(smem_addr(&ctl->afull[s]), kGatherWarps);
+            // gather mode: + the leader's gather threads (on landing) + the peer's relay
+            mbar_init(smem_addr(&ctl->full[s]), p.gather ? 1 + 32 * kGatherWarps + 1 : 1);
+            mbar_init(smem_addr(&ctl->afull[s]), 32 * kGatherWarps);  // the peer's gather threads
             mbar_init(smem_addr(&ctl->empty[s]), 1);  // the leader's multicast commit
         }
         for (int a = 0; a < 2; ++a) {
@@ -1781,7 +1773,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && leader) pair_mma_role<STAGES, BN>(p, ctl, sA, sB, tmem_base, w);
+        if (lane == 0 && leader) {
+            if (p.gather) pair_mma_role<STAGES, BN, true>(p, ctl, sA, sB, tmem_base, w);
+            else pair_mma_role<STAGES, BN, false>(p, ctl, sA, sB, tmem_base, w);
+        }
         else if (lane == 0 && p.gather) pair_relay_role<STAGES>(p, ctl, w, lead);
         __syncwarp();
     } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {

@@ -31,7 +31,6 @@ struct moe_plan_s {
     int half_tiles = 0;  // single-CTA plans: 1 = small schedules run as half-width tiles
     int scatter_parts = 1;  // scatter order: parts per expert (chunk-major), nch E <= kMaxE
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
-    bool single_ready = false;  // automatic pair plans: single-CTA kernel attributes set (direct gather)
     unsigned long long* trace = nullptr;  // per-CTA trace records (moe_set_trace), or null
     // tensor maps, re-encoded only when the buffers change
     std::mutex mu;
@@ -492,28 +491,7 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     prm.half_tiles = (glu || combine) ? 0 : plan->half_tiles;
     prm.nch = plan->scatter_parts;
     cudaError_t lerr;
-    if (gather && plan->pair && plan->shape.tile_m != 256) {
-        // The direct gather of an automatic pair plan runs in the single-CTA kernel with
-        // 256-wide tiles: there it moves its rows about twice as fast as on CTA pairs, whose
-        // peer must signal every gathered stage to the leader across the pair.  A plan that
-        // asks for CTA pairs (tile_m = 256) gets the pair version.
-        const size_t smem = dispatch_gemm_smem_bytes(256, 4);
-        {
-            std::lock_guard<std::mutex> lock(plan->mu);
-            if (!plan->single_ready) {
-                if (dispatch_gemm_prepare_attributes(256, 4, smem) != cudaSuccess) {
-                    cudaGetLastError();
-                    return MOE_ERR_CUDA;
-                }
-                plan->single_ready = true;
-            }
-        }
-        prm.tile_n = 256;
-        prm.n_tiles = (plan->N + 255) / 256;
-        const int grid = plan->shape.num_ctas != 0 ? std::min(plan->shape.num_ctas, plan->sm_count)
-                                                   : plan->sm_count;
-        lerr = launch_dispatch_gemm(prm, grid, 4, smem, static_cast<cudaStream_t>(stream));
-    } else if (plan->pair) {
+    if (plan->pair) {
         lerr = launch_dispatch_gemm_pair(prm, plan->num_ctas, plan->smem, static_cast<cudaStream_t>(stream));
     } else {
         lerr = launch_dispatch_gemm(prm, plan->num_ctas, plan->stages, plan->smem,

@@ -218,6 +218,16 @@ __device__ __forceinline__ void cp_async16_cg_zfill(uint32_t dst, const void* sr
                  : "memory");
 }
 
+// one arrival on a barrier of this CTA once every cp.async this thread has issued so
+// far has landed (.noinc: the barrier's expected count includes this arrival)
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -394,6 +404,13 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 // arrive on an mbarrier given by its shared::cluster address (this CTA or the peer)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// arrive on the peer CTA's mbarrier with release semantics at CTA scope: the form for a
+// per-stage signal on the critical path (the cluster-scope release above costs about a
+// microsecond per arrival, measured)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // wait on a local mbarrier whose arrivals may come from the peer CTA
