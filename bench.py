@@ -57,10 +57,11 @@ def _args(argv=None):
     ap.add_argument("--workloads", default="others",
                     help="other configurations measured in the same run: 'others' (every other "
                          "workload), 'none', or a comma-separated list")
-    ap.add_argument("--kernel-only", choices=["fused", "grouped"], default=None,
+    ap.add_argument("--kernel-only", choices=["fused", "grouped", "gather"], default=None,
                     help="profiling case: after the warm-up, run only `--steps` launches of the fused "
-                         "kernel (moe_dispatch_gemm) or of the GEMM alone on the receive rows in place "
-                         "(moe_grouped_gemm), L2 flushed between them, print their median and exit")
+                         "kernel (moe_dispatch_gemm), of the GEMM alone on the receive rows in place "
+                         "(moe_grouped_gemm) or of the direct gather (moe_gather_gemm), L2 flushed "
+                         "between them, print their median and exit")
     ap.add_argument("--ffn", choices=["auto", "on", "off"], default="auto",
                     help="also time the gated (SwiGLU) expert FFN with F = N (auto: Mixtral-shaped only)")
     return ap.parse_args(argv)
@@ -422,8 +423,15 @@ def measure_workload(wl, K: int, warmup: int, dev, stream, flush, l2: str = "flu
     if rc != 0:
         raise SystemExit(f"{wl.name}: device status after the combine timing: {st}")
     del comb_out
+    # the direct gather on the same plan (no receive buffers, the same bits)
+    gather_ms = median_ms(lambda: binding.gather_gemm(plan, x, W, bufs, stream))
+    rc, st = binding.moe_read_status(bufs.status, stream)
+    if rc != 0:
+        raise SystemExit(f"{wl.name}: device status after the gather timing: {st}")
     _, _, scatter_bytes = algorithmic_work(wl, touched)
     peaks = _peaks()
+    # the gather's own algorithmic bytes: x once, the touched weights, Y (no receive rows)
+    gather_bytes = wl.T * wl.d * 2 + touched * wl.d * wl.N * 2 + wl.S * wl.N * 4
     roof = roofline_of(wl, touched, statistics.mean(dg_ms) / 1000.0, plan.info, peaks)
     out = {
         "config": {**wl.describe(), "tile_m": plan.info["tile_m"], "tile_n": plan.info["tile_n"],
@@ -445,6 +453,13 @@ def measure_workload(wl, K: int, warmup: int, dev, stream, flush, l2: str = "flu
                     "fused_ms": fused_comb_ms,
                     "note": "fused kernel + moe_combine against moe_dispatch_gemm_combine; 10 launches "
                             "each, L2 flushed; not in step_ms"},
+        "direct_gather": {"ms": gather_ms, "tflops": wl.flops / (gather_ms * 1e9),
+                          "frac_bf16_peak": wl.flops / (gather_ms * 1e9) / peaks[1],
+                          "gbs": gather_bytes / (gather_ms * 1e6),
+                          "frac_hbm": gather_bytes / (gather_ms * 1e6) / peaks[0],
+                          "speedup_vs_dispatch": statistics.median(dg_ms) / gather_ms,
+                          "note": "moe_gather_gemm on the same plan (A rows copied from x, no receive "
+                                  "buffers, Y bit-identical); 10 launches, L2 flushed; not in step_ms"},
         "clocks": clk.summary(),
         "gpu_launches": launches_per_step(wl) * K,
     }
@@ -660,6 +675,8 @@ def run_kernel_only(args, wl):
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     if args.kernel_only == "fused":
         launch = lambda: binding.dispatch_gemm(plan, x, W, bufs, stream)
+    elif args.kernel_only == "gather":
+        launch = lambda: binding.gather_gemm(plan, x, W, bufs, stream)
     else:
         if wl.R != 1:
             raise SystemExit("--kernel-only grouped needs one rank buffer (R = 1)")
@@ -996,9 +1013,10 @@ def run_ours(args, wl):
         "direct_gather": {"ms": gather_ms, "tflops": flops / (gather_ms * 1e9),
                           "dispatch_gemm_ms": statistics.median(dg_ms),
                           "speedup_vs_dispatch": statistics.median(dg_ms) / gather_ms,
-                          "note": "moe_gather_gemm: A rows copied from x by perm straight into the "
-                                  "GEMM's shared memory by cp.async warps, no receive buffers (256-wide single-CTA tiles "
-                                  "on an automatic pair plan); "
+                          "frac_bf16_peak": flops / (gather_ms * 1e9) / _peaks()[1],
+                          "note": "moe_gather_gemm on the same plan: A rows copied from x by perm straight "
+                                  "into the GEMM's shared memory by cp.async warps, no receive buffers, no "
+                                  "scatter phase, Y bit-identical to the dispatch; "
                                   "20 launches, L2 flushed; not in value"},
         "y_bf16": {"ms": ybf16_ms, "tflops": flops / (ybf16_ms * 1e9),
                    "note": "moe_dispatch_gemm with out_dtype = MOE_OUT_BF16 (Y rounded once to bf16, "
