@@ -1088,7 +1088,7 @@ __device__ void gather_a_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t
         if (lane == 0) {
             const uint32_t se = smem_addr(&ctl->sempty[slot]);
             if (leader) mbar_arrive(se);
-            else mbar_arrive_cluster(mapa_shared(se, lead));
+            else mbar_arrive_remote(mapa_shared(se, lead));
         }
         if (++slot == kRing) {
             slot = 0;
@@ -1158,7 +1158,7 @@ __device__ void pair_relay_role(const DispatchGemmParams& p, SmemCtl* ctl, const
     for (;;) {
         if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 31, true, true)) return;
         const int e = ctl->ring[slot].e;
-        mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
+        mbar_arrive_remote(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
         if (++slot == kRing) {
             slot = 0;
             sphase ^= 1u;
@@ -1435,7 +1435,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 return true;  // not published yet
             }
             ti = ctl->ring[slot];
-            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
+            mbar_arrive_remote(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
         }
         if (++slot == kRing) {
             slot = 0;
@@ -1632,7 +1632,7 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         if (lane == 0) {
             const uint32_t se = smem_addr(&ctl->sempty[slot]);
             if (leader) mbar_arrive(se);
-            else mbar_arrive_cluster(mapa_shared(se, lead));
+            else mbar_arrive_remote(mapa_shared(se, lead));
         }
         if (++slot == kRing) {
             slot = 0;
@@ -1660,7 +1660,7 @@ __device__ void pair_epilogue_role(const DispatchGemmParams& p, SmemCtl* ctl, ui
         if (lane == 0) {
             const uint32_t te = smem_addr(&ctl->tempty[acc]);
             if (leader) mbar_arrive(te);
-            else mbar_arrive_cluster(mapa_shared(te, lead));
+            else mbar_arrive_remote(mapa_shared(te, lead));
         }
         if (p.combine)  // an M=128 tile's two CTAs each publish their 64-row half
             combine_publish(p, ti.rows > 0 ? ti.mtile : -1, ti.n, ti.m128 ? (leader ? 0 : 1) : 0, w.epoch);

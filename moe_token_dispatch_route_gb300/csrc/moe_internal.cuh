@@ -407,8 +407,9 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
 }
 
 // arrive on the peer CTA's mbarrier with release semantics at CTA scope: the form for a
-// per-stage signal on the critical path (the cluster-scope release above costs about a
-// microsecond per arrival, measured)
+// signal that hands a buffer (a stage, a ring slot, an accumulator) back or on, where the
+// data itself needs no cluster-scope ordering (the cluster-scope release above costs about
+// a microsecond per arrival, measured)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
