@@ -93,6 +93,9 @@ struct SmemCtl {
     PieceRec piece[kThreads / 32][kMaxPieceBufs];  // scatter: per-warp ring of staged pieces
 };
 
+static_assert(sizeof(TileInfo) % 8 == 0, "tile descriptions move in 8-byte asynchronous stores");
+static_assert(offsetof(SmemCtl, ring) % 8 == 0, "ring slots must be 8-byte aligned");
+
 struct Waiter {
     volatile int* abort;
     int32_t* status;
@@ -1396,10 +1399,11 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
 
-    // Leader: claim a pair tile and publish both halves' descriptions (the peer's
-    // through distributed shared memory).  Peer: take the next description from its
+    // Leader: claim a pair tile and publish both halves' descriptions (the peer's by
+    // asynchronous stores into its ring slot that complete its ring barrier).  Peer: take the next description from its
     // ring; with `block` false it only takes one that is already there.  Both read
     // the ready flag of their own half.
+    bool armed = false;  // peer: this use of the ring slot is armed
     auto next_tile = [&](TileInfo& ti, uint32_t& flag, bool block, bool& got) -> bool {
         got = false;
         if (leader) {
@@ -1421,14 +1425,22 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 pair_half_info(p, mt_base, e, m2, n, 1, other);
             }
             ctl->ring[slot] = ti;
+            // the peer's half: asynchronous stores whose bytes complete the peer's ring
+            // barrier (armed by the peer's TMA thread), so the description is visible there
+            // when the barrier completes, without a cluster-scope release
             const int* o = reinterpret_cast<const int*>(&other);
             const uint32_t remote = mapa_shared(smem_addr(&ctl->ring[slot]), peer);
+            const uint32_t rbar = mapa_shared(smem_addr(&ctl->sfull[slot]), peer);
 #pragma unroll
-            for (int i = 0; i < (int)(sizeof(TileInfo) / 4); ++i) st_cluster_u32(remote + 4 * i, (uint32_t)o[i]);
+            for (int i = 0; i < (int)(sizeof(TileInfo) / 8); ++i)
+                st_async_v2(remote + 8 * i, (uint32_t)o[2 * i], (uint32_t)o[2 * i + 1], rbar);
             mbar_arrive(smem_addr(&ctl->sfull[slot]));
-            mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->sfull[slot]), peer));
         } else {
             const uint32_t sf = smem_addr(&ctl->sfull[slot]);
+            if (!armed) {  // once per use of the slot: this thread's arrival + the description's bytes
+                mbar_arrive_expect_tx(sf, (uint32_t)sizeof(TileInfo));
+                armed = true;
+            }
             if (block) {
                 if (!wait_bar(sf, sphase, w, 22, true, true)) return false;
             } else if (!mbar_try_wait_cluster(sf, sphase)) {
@@ -1437,6 +1449,7 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
             ti = ctl->ring[slot];
             mbar_arrive_remote(mapa_shared(smem_addr(&ctl->sempty[slot]), lead));
         }
+        armed = false;
         if (++slot == kRing) {
             slot = 0;
             sphase ^= 1u;

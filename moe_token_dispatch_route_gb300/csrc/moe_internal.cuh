@@ -414,6 +414,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+// 8 bytes into the peer CTA's shared memory, counted as 8 transaction bytes on the peer's
+// mbarrier `mbar_cluster` once they are visible there
+__device__ __forceinline__ void st_async_v2(uint32_t addr_cluster, uint32_t a, uint32_t b, uint32_t mbar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr_cluster), "r"(a), "r"(b), "r"(mbar_cluster) : "memory");
+}
+
 // wait on a local mbarrier whose arrivals may come from the peer CTA
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
