@@ -1400,9 +1400,9 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
     for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
 
     // Leader: claim a pair tile and publish both halves' descriptions (the peer's by
-    // asynchronous stores into its ring slot that complete its ring barrier).  Peer: take the next description from its
-    // ring; with `block` false it only takes one that is already there.  Both read
-    // the ready flag of their own half.
+    // asynchronous stores into its ring slot that complete its ring barrier).  Peer:
+    // take the next description from its ring; with `block` false it only takes one that
+    // is already there.  Both read the ready flag of their own half.
     bool armed = false;  // peer: this use of the ring slot is armed
     auto next_tile = [&](TileInfo& ti, uint32_t& flag, bool block, bool& got) -> bool {
         got = false;
