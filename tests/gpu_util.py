@@ -71,6 +71,21 @@ def check_Y(Y: np.ndarray, Yref: np.ndarray):
     return float(err.max()), rms
 
 
+def check_after_bf16_rounding(Y: np.ndarray, Yref: np.ndarray, abs_bound: np.ndarray):
+    """A product whose left operand the GPU rounded to bf16 from its fp32 value and the
+    oracle from its fp64 one (SwiGLU's H before the down projection).  Where the unrounded
+    value sits within fp32 error of a bf16 rounding midpoint the two round one bf16 ulp
+    apart, at most 2^-7 of its magnitude; so each element may differ by 2^-7 times
+    `abs_bound` (the oracle's |H| . |W| for that element) beyond the fp32 accumulation
+    error (1e-4 RMS)."""
+    assert Y.shape == Yref.shape
+    assert np.isfinite(Y).all(), "unwritten (NaN) or non-finite output"
+    rms = float(np.sqrt(np.mean(Yref ** 2))) if Yref.size else 0.0
+    bound = 2.0 ** -7 * abs_bound + 1e-4 * rms
+    worst = np.unravel_index(np.argmax(np.abs(Y - Yref) - bound), Y.shape) if Y.size else None
+    assert (np.abs(Y - Yref) <= bound).all(), (worst, float(Y[worst]), float(Yref[worst]), float(bound[worst]))
+
+
 def sample_rows_cols(ref, N, tile_m=128, tile_n=256, n_random=48, seed=0, row_block=32, col_block=64):
     """Rows and columns of a sampled check of Y that touches every output tile.
 

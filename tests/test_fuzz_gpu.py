@@ -18,7 +18,7 @@ import torch
 
 import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
-from tests.gpu_util import check_recv, check_route, check_Y, run_path
+from tests.gpu_util import check_after_bf16_rounding, check_recv, check_route, check_Y, run_path
 
 pytestmark = pytest.mark.gpu
 
@@ -163,6 +163,9 @@ def test_random_shapes_gated_ffn_chain(i):
     rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], k)
     Href = oracle.swiglu(oracle.grouped_gemm(rows, workloads.bf16_bits(W1), ref["offsets"]))
     _check_H(bu.H, Href)
-    Y2 = oracle.grouped_gemm(oracle.round_bf16(Href), workloads.bf16_bits(W2), ref["offsets"])
-    check_Y(bd.Y.cpu().double().numpy(), Y2)
-    check_Y(out.cpu().double().numpy(), oracle.combine(Y2, ref["topk_w"], ref["dest"]))
+    Hb, W2b = oracle.round_bf16(Href), workloads.bf16_bits(W2)
+    Y2 = oracle.grouped_gemm(Hb, W2b, ref["offsets"])
+    absHW = oracle.grouped_gemm(Hb & 0x7FFF, W2b & 0x7FFF, ref["offsets"])  # |H| . |W2|
+    check_after_bf16_rounding(bd.Y.cpu().double().numpy(), Y2, absHW)
+    check_after_bf16_rounding(out.cpu().double().numpy(), oracle.combine(Y2, ref["topk_w"], ref["dest"]),
+                              oracle.combine(absHW, np.abs(ref["topk_w"]), ref["dest"]))

@@ -18,8 +18,8 @@ import torch
 
 import oracle
 from moe_token_dispatch_route_gb300 import binding, workloads
-from tests.gpu_util import (TOL_FRO, TOL_MAX_REL_RMS, check_recv, check_route, check_Y, oracle_grid,
-                            sample_rows_cols)
+from tests.gpu_util import (TOL_FRO, TOL_MAX_REL_RMS, check_after_bf16_rounding, check_recv, check_route,
+                            check_Y, oracle_grid, sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -215,8 +215,11 @@ def test_swiglu_ffn_chain(tile_m):
     rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], k)
     Href = oracle.swiglu(oracle.grouped_gemm(rows, workloads.bf16_bits(W1), ref["offsets"]))
     check_H(bu.H, Href)
-    Y2 = oracle.grouped_gemm(oracle.round_bf16(Href), workloads.bf16_bits(W2), ref["offsets"])
-    check_Y(out.cpu().double().numpy(), oracle.combine(Y2, ref["topk_w"], ref["dest"]))
+    Hb, W2b = oracle.round_bf16(Href), workloads.bf16_bits(W2)
+    Y2 = oracle.grouped_gemm(Hb, W2b, ref["offsets"])
+    absHW = oracle.grouped_gemm(Hb & 0x7FFF, W2b & 0x7FFF, ref["offsets"])  # |H| . |W2|
+    check_after_bf16_rounding(out.cpu().double().numpy(), oracle.combine(Y2, ref["topk_w"], ref["dest"]),
+                              oracle.combine(absHW, np.abs(ref["topk_w"]), ref["dest"]))
 
 
 # -------------------------------------------------- full size, sampled entries
