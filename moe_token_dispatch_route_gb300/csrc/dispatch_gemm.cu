@@ -1510,16 +1510,18 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
                 if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::kStageBytes);
                 tma_load_2d_pair(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             }
-            if (p.b3d) {  // boxes 2h and 2h + 1 are adjacent chunks: one copy each h
+            if (GATHER) {  // in the dispatch and grouped modes warp 2 issues the B boxes
+                if (p.b3d) {  // boxes 2h and 2h + 1 are adjacent chunks: one copy each h
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h)
-                    tma_load_3d_pair(smem_addr(sB + stage * C::kBBytes + 16384 * h), &p.b3_map, fb, 0,
-                                     brow + kb * kTileK, bcol[2 * h] >> 6);
-            } else {
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d_pair(smem_addr(sB + stage * C::kBBytes + 16384 * h), &p.b3_map, fb, 0,
+                                         brow + kb * kTileK, bcol[2 * h] >> 6);
+                } else {
 #pragma unroll
-                for (int b = 0; b < 2 * C::kHalves; ++b)
-                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
-                                     brow + kb * kTileK);
+                    for (int b = 0; b < 2 * C::kHalves; ++b)
+                        tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb,
+                                         bcol[b], brow + kb * kTileK);
+                }
             }
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
@@ -1540,6 +1542,60 @@ __device__ void pair_tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const i
         for (int s = 0; s < STAGES; ++s)
             if (last_phase[s] >= 0)
                 wait_bar(smem_addr(&ctl->full[s]), (uint32_t)last_phase[s], w, 24, false, true);
+    }
+}
+
+// B loads of the dispatch and grouped modes (lane 0 of warp 2 of both CTAs of a pair):
+// follows the schedule ring like the epilogue and issues this CTA's B boxes of every
+// k-block once the stage is free, so the TMA thread issues only A.  A thread issuing a
+// k-block's copies is slowed by each one it issues (about 0.26 us per k-block measured for
+// three copies), and in this latency-bound pipeline two issuing threads keep the stages
+// fuller (Mixtral-shaped dispatch 7% faster).  The leader's TMA thread arms each stage
+// for all its bytes; B's may land first (the transaction count goes below zero for a time).
+template <int STAGES, int BN>
+__device__ void pair_tma_b_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sB, const Waiter& w,
+                                bool leader, uint32_t lead) {
+    using C = PairCfg<STAGES, BN>;
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    for (;;) {
+        if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 33, true, true)) return;
+        const TileInfo ti = ctl->ring[slot];
+        const uint32_t se = smem_addr(&ctl->sempty[slot]);
+        if (leader) mbar_arrive(se);
+        else mbar_arrive_remote(mapa_shared(se, lead));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.e < 0) return;
+        int bcol[2 * C::kHalves];
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) bcol[2 * h + b] = b_box_col(p, ti.n, C::kBN, 4 * h + (leader ? 0 : 2) + b);
+        const int brow = ti.e * p.d;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 34, true, true)) return;
+            const uint32_t fb = mapa_shared(smem_addr(&ctl->full[stage]), lead);
+            if (p.b3d) {
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h)
+                    tma_load_3d_pair(smem_addr(sB + stage * C::kBBytes + 16384 * h), &p.b3_map, fb, 0,
+                                     brow + kb * kTileK, bcol[2 * h] >> 6);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 2 * C::kHalves; ++b)
+                    tma_load_2d_pair(smem_addr(sB + stage * C::kBBytes + 8192 * b), &p.b_map, fb, bcol[b],
+                                     brow + kb * kTileK);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
     }
 }
 
@@ -1721,7 +1777,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&ctl->sfull[r]), 1);
             // leader: own MMA thread + 4 epilogue warps + the peer's TMA thread and 4 epilogue
             // warps (+ both CTAs' gather warps and the peer's relay in the gather mode)
-            mbar_init(smem_addr(&ctl->sempty[r]), 10 + (p.gather ? 2 * kGatherWarps + 1 : 0));
+            mbar_init(smem_addr(&ctl->sempty[r]), 10 + (p.gather ? 2 * kGatherWarps + 1 : 2));
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -1794,6 +1850,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
         gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0, true, leader, lead);
+    } else if (!p.gather && warp == 2) {
+        if (lane == 0) pair_tma_b_role<STAGES, BN>(p, ctl, sB, w, leader, lead);
+        __syncwarp();
     } else if (warp >= kEpiWarp0) {
         pair_epilogue_role<STAGES, BN>(p, ctl, tmem_base, w, leader, lead,
                                    epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats, mt_base);
