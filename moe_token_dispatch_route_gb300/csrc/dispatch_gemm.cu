@@ -909,11 +909,13 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
                 mbar_arrive_expect_tx(fb, C::kABytes + b_bytes);
                 tma_load_2d(smem_addr(sA + stage * C::kABytes), amap, fb, kb * kTileK, cur.arow);
             }
+            if (p.gather) {  // otherwise warp 2 issues the B boxes (tma_b_role)
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-                if (j < nbox)
-                    tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
-                                b_box_col(p, cur.n, BN, j) + bshift, brow + kb * kTileK);
+                for (int j = 0; j < BN / 64; ++j)
+                    if (j < nbox)
+                        tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
+                                    b_box_col(p, cur.n, BN, j) + bshift, brow + kb * kTileK);
+            }
             last_phase[stage] = (int)phase;
             if (++stage == STAGES) {
                 stage = 0;
@@ -928,6 +930,44 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
 #pragma unroll
     for (int s = 0; s < STAGES; ++s)
         if (last_phase[s] >= 0) wait_bar(smem_addr(&ctl->full[s]), (uint32_t)last_phase[s], w, 3, false);
+}
+
+// B loads of a single-CTA tile outside the gather mode (lane 0 of warp 2): follows the
+// schedule ring and issues the tile's B boxes (or one half's) of every k-block once the
+// stage is free; the TMA thread issues A and arms the stage for all its bytes.
+template <int BN, int STAGES>
+__device__ void tma_b_role(const DispatchGemmParams& p, SmemCtl* ctl, uint8_t* sB, const Waiter& w) {
+    using C = Cfg<BN, STAGES>;
+    int stage = 0;
+    uint32_t phase = 0;
+    int slot = 0;
+    uint32_t sphase = 0;
+    for (;;) {
+        if (!wait_bar(smem_addr(&ctl->sfull[slot]), sphase, w, 35)) return;
+        const TileInfo ti = ctl->ring[slot];
+        mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (++slot == kRing) {
+            slot = 0;
+            sphase ^= 1u;
+        }
+        if (ti.rows < 0) return;
+        const int nbox = ti.half ? BN / 128 : BN / 64;
+        const int bshift = ti.half == 2 ? BN / 2 : 0;
+        const int brow = ti.e * p.d;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1u, w, 36)) return;
+            const uint32_t fb = smem_addr(&ctl->full[stage]);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                if (j < nbox)
+                    tma_load_2d(smem_addr(sB + stage * C::kBBytes + j * 8192), &p.b_map, fb,
+                                b_box_col(p, ti.n, BN, j) + bshift, brow + kb * kTileK);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
 }
 
 template <int BN, int STAGES, bool GATHER>
@@ -1207,7 +1247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < kRing; ++r) {
             mbar_init(smem_addr(&ctl->sfull[r]), 1);
             // MMA thread + 4 epilogue warps (+ the gather warps)
-            mbar_init(smem_addr(&ctl->sempty[r]), 1 + 4 + (p.gather ? kGatherWarps : 0));
+            mbar_init(smem_addr(&ctl->sempty[r]), 1 + 4 + (p.gather ? kGatherWarps : 1));
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -1269,6 +1309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (p.gather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
         gather_a_role<STAGES>(p, ctl, sA, w, warp - kGatherWarp0, false, true, 0);
+    } else if (!p.gather && warp == 2) {
+        if (lane == 0) tma_b_role<BN, STAGES>(p, ctl, sB, w);
+        __syncwarp();
     } else if (warp >= kEpiWarp0) {
         epilogue_role<BN, STAGES>(p, ctl, tmem_base, w, epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats, mt_base);
     }
