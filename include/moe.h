@@ -127,6 +127,12 @@ typedef struct moe_plan_info {
                                          tiles runs each tile as two half-width tiles
                                          (the same bits; single-CTA plans of tile_n 128
                                          or 256); 0: whole tiles only                   */
+    int32_t background_scatter;       /* CTA-pair plans, moe_dispatch_gemm: > 0 when every
+                                         warp scatters only the rows of the first experts
+                                         (those holding this many pair tiles) before the
+                                         GEMM and warp 3 of each CTA copies the rest beside
+                                         it (layers of N >= 8192); 0: the whole scatter
+                                         first.  Same bits either way                     */
 } moe_plan_info_t;
 
 /*

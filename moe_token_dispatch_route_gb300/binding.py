@@ -58,7 +58,7 @@ class PlanInfo(ctypes.Structure):
         ("stages", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("producer_ctas", ctypes.c_int32),
         ("sm_count", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("max_mtiles", ctypes.c_int32),
         ("route_blocks", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
-        ("half_tiles", ctypes.c_int32),
+        ("half_tiles", ctypes.c_int32), ("background_scatter", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

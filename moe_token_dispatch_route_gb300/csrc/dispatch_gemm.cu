@@ -18,7 +18,11 @@
 //    into the rank buffers with 16-byte loads and stores, 4 rows per work
 //    unit, in the order the GEMM consumes them.  The last unit of each
 //    128-row tile publishes the tile's ready flag (release store of the call's
-//    epoch).  Then the CTA joins the GEMM role.
+//    epoch).  Then the CTA joins the GEMM role.  CTA pairs on wide layers
+//    (N >= 8192: few rows per second feed the GEMM) copy only the first
+//    experts' rows this way, enough for the first two waves of tiles; warp 3
+//    of every CTA then copies the rest through registers beside the GEMM,
+//    publishing the same flags.
 //  * GEMM role, warp-specialised: warp 0 lane 0 claims tiles from a
 //    workspace counter (expert-major, then column tile, then row tile),
 //    waits for the row tile's flag (acquire, then a generic->async proxy
@@ -319,10 +323,10 @@ __device__ void cursor_select(UnitCursor& u) {
 
 // first unit of the walk
 __device__ void cursor_init(UnitCursor& u, const DispatchGemmParams& p, const int* unit_base, int first,
-                            int stride, uint32_t epoch, int lane) {
+                            int stride, int total, uint32_t epoch, int lane) {
     u.c = first;
     u.stride = stride;
-    u.total = unit_base[p.nch * p.E];
+    u.total = total;
     u.slot = 0;
     cursor_fetch_batch(u, p, unit_base, epoch, lane);
     cursor_select(u);
@@ -385,7 +389,7 @@ __device__ void publish_units(const DispatchGemmParams& p, const int* mt_base, c
 // least two piece buffers), all inside the stage area
 __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
                              int role, uint32_t epoch, uint8_t* staging, SmemCtl* ctl,
-                             int slots_per_lane) {
+                             int slots_per_lane, int end_units) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = p.producer_ctas * (kThreads / 32);
     const int nvec = p.d / 8;
@@ -397,7 +401,7 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
     PieceRec* ring = ctl->piece[warp];
 
     UnitCursor L;
-    cursor_init(L, p, unit_base, role * (kThreads / 32) + warp, nwarps, epoch, lane);
+    cursor_init(L, p, unit_base, role * (kThreads / 32) + warp, nwarps, end_units, epoch, lane);
 
     int pend_e[kPublishBatch], pend_j[kPublishBatch];
     int npend = 0;
@@ -475,6 +479,73 @@ __device__ void scatter_role(const DispatchGemmParams& p, const int* mt_base, co
     cp_async_wait<0>();
     // the staging area becomes TMA (async-proxy) destination again
     fence_proxy_async_smem();
+}
+
+// Background scatter (one warp of a CTA, beside the GEMM roles): the units
+// [first, total) in steps of `stride`, each row copied through registers with
+// kBgVecs 16-byte loads per lane in flight, then stored; finished units are
+// counted in and their tiles' flags released exactly as the all-warps scatter does.
+constexpr int kBgVecs = 16;
+__device__ void scatter_background(const DispatchGemmParams& p, const int* mt_base, const int* unit_base,
+                                   int first, int stride, int total, uint32_t epoch) {
+    const int lane = threadIdx.x & 31;
+    const int nvec = p.d / 8;
+    UnitCursor L;
+    cursor_init(L, p, unit_base, first, stride, total, epoch, lane);
+    int pend_e[kPublishBatch], pend_j[kPublishBatch];
+    int npend = 0;
+    while (!L.done) {
+        int tr[kRowsPerChunk], lr[kRowsPerChunk];
+#pragma unroll
+        for (int r = 0; r < kRowsPerChunk; ++r) {
+            tr[r] = -1;
+            lr[r] = 0;
+            if (r < L.nrows) cursor_row(L, r, tr[r], lr[r]);
+        }
+        uint16_t* rbuf = p.recv[L.rank];
+        const int items = L.nrows * nvec;
+        for (int f0 = 0; f0 < items; f0 += 32 * kBgVecs) {
+            uint4 t[kBgVecs];
+#pragma unroll
+            for (int i = 0; i < kBgVecs; ++i) {
+                const int f = f0 + lane + 32 * i;
+                const int r = f / nvec;
+                int tok = -1;
+#pragma unroll
+                for (int q = 0; q < kRowsPerChunk; ++q)
+                    if (r == q) tok = tr[q];
+                if (f < items && tok >= 0)
+                    t[i] = ld_nc_na_v4(reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.d) + (f - r * nvec));
+            }
+#pragma unroll
+            for (int i = 0; i < kBgVecs; ++i) {
+                const int f = f0 + lane + 32 * i;
+                const int r = f / nvec;
+                int tok = -1, loc = 0;
+#pragma unroll
+                for (int q = 0; q < kRowsPerChunk; ++q)
+                    if (r == q) {
+                        tok = tr[q];
+                        loc = lr[q];
+                    }
+                if (f < items && tok >= 0)
+                    reinterpret_cast<uint4*>(rbuf + (size_t)loc * p.d)[f - r * nvec] = t[i];
+            }
+        }
+        pend_e[npend] = L.e;
+        pend_j[npend] = L.j;
+        ++npend;
+        cursor_next(L, p, unit_base, epoch, lane);
+        if (npend == kPublishBatch || (L.done && npend > 0)) {
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                publish_units(p, mt_base, pend_e, pend_j, npend, epoch);
+            }
+            npend = 0;
+        }
+    }
 }
 
 // Epilogue staging: each epilogue warp turns a 32-row x 32-column fp32 block (one row per
@@ -1289,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (role < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl, C::kScatterSlots);
+        scatter_role(p, mt_base, unit_base, role, epoch, sA, ctl, C::kScatterSlots, unit_base[p.nch * p.E]);
         __syncthreads();
         if (tid == 0) {
             const unsigned long long t = global_timer_ns();
@@ -1866,10 +1937,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const long long pipe_timeout = p.timeout_ns * 2 > 500000000LL ? p.timeout_ns * 2 : 500000000LL;
     const Waiter w{&ctl->abort, p.status, p.timeout_ns, pipe_timeout, epoch};
+    // the all-warps scatter covers the units before head_units; warp 3 copies the rest
+    const int total_units = unit_base[p.nch * p.E];
+    int head_units = total_units;
+    if (p.bg_head > 0 && p.nch == 1) {
+        int h = 0;
+        while (h < p.E && pt_base[h] * p.n_tiles < p.bg_head) ++h;
+        head_units = unit_base[h];
+    }
     if (scatter_index < p.producer_ctas) {
         unsigned long long* w64 = reinterpret_cast<unsigned long long*>(p.hdr);
         if (tid == 0) atomicMax(w64 + kHdrScatterInvStart / 2, ~(unsigned long long)global_timer_ns());
-        scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl, C::kScatterSlots);
+        scatter_role(p, mt_base, unit_base, scatter_index, epoch, sA, ctl, C::kScatterSlots, head_units);
         __syncthreads();
         if (tid == 0) {
             const unsigned long long t = global_timer_ns();
@@ -1896,6 +1975,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (!p.gather && warp == 2) {
         if (lane == 0) pair_tma_b_role<STAGES, BN>(p, ctl, sB, w, leader, lead);
         __syncwarp();
+    } else if (warp == 3) {
+        if (head_units < total_units) {
+            scatter_background(p, mt_base, unit_base, head_units + scatter_index, gridDim.x, total_units, epoch);
+            if (lane == 0)
+                atomicMax(reinterpret_cast<unsigned long long*>(p.hdr) + kHdrScatterEnd / 2, global_timer_ns());
+        }
     } else if (warp >= kEpiWarp0) {
         pair_epilogue_role<STAGES, BN>(p, ctl, tmem_base, w, leader, lead,
                                    epi_tiles + (warp - kEpiWarp0) * kEpiWarpFloats, mt_base);

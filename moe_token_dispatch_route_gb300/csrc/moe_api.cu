@@ -29,6 +29,8 @@ struct moe_plan_s {
     int skip_publish = -1;
     int band = 0;
     int half_tiles = 0;  // single-CTA plans: 1 = small schedules run as half-width tiles
+    int bg_head = -1;    // CTA pairs: pair tiles the all-warps scatter covers before the GEMM
+                         //   (the rest is copied beside it); -1 auto by output width, 0 off
     int scatter_parts = 1;  // scatter order: parts per expert (chunk-major), nch E <= kMaxE
     bool pair = false;  // CTA-pair mode: clusters of 2, 256 x 256 tiles, tcgen05 cta_group::2
     unsigned long long* trace = nullptr;  // per-CTA trace records (moe_set_trace), or null
@@ -154,6 +156,19 @@ bool plan_route_shape(moe_plan_t plan, int* T, int* E, int* k, int* route_blocks
 }
 }  // namespace moe
 
+// CTA pairs on wide layers: every warp scatters only the rows of the first experts that hold
+// the first two waves of pair tiles (num_ctas pair tiles), then joins the GEMM, while warp 3 of
+// every CTA copies the remaining rows beside it.  A GEMM of `out_cols` output columns needs
+// out_cols flops per byte of A, so at the bf16 peak a layer of at least kBgMinCols columns
+// consumes rows at under 0.25 TB/s, which those warps (about 0.3 TB/s measured) keep ahead
+// of; narrower layers scatter everything first.  Returns the head in pair tiles, 0 off.
+constexpr int kBgMinCols = 8192;
+static int bg_head_for(const moe_plan_s* plan, int out_cols) {
+    if (!plan->pair) return 0;
+    if (plan->bg_head >= 0) return plan->bg_head;
+    return out_cols >= kBgMinCols ? plan->num_ctas : 0;
+}
+
 extern "C" {
 
 const char* moe_status_string(moe_status_t s) {
@@ -265,6 +280,8 @@ moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan, si
     if (!p->pair && (p->tile_n == 128 || p->tile_n == 256)) p->half_tiles = 1;
     if (const char* env = std::getenv("MOE_HALF_TILES"))  // tuning override: 0 never, 2 always
         p->half_tiles = p->half_tiles ? std::max(0, std::min(2, std::atoi(env))) : 0;
+    // tuning override for sweeps and tests: the background scatter's head (0 off)
+    if (const char* env = std::getenv("MOE_BG_HEAD")) p->bg_head = std::max(0, std::atoi(env));
     // The scatter walks each expert's rows in token-ordered parts of about 1024 tokens (at
     // most 16), part-major, so that a token's k copies are made while its x row is in L2.
     p->scatter_parts = std::max(1, std::min(std::min(16, kMaxE / p->E), p->T / 1024));
@@ -312,6 +329,7 @@ moe_status_t moe_plan_info(moe_plan_t plan, moe_plan_info_t* info) {
     info->route_blocks = plan->route_blocks;
     info->workspace_bytes = (int64_t)plan->ws.total;
     info->half_tiles = plan->half_tiles;
+    info->background_scatter = bg_head_for(plan, plan->N);
     return MOE_OK;
 }
 
@@ -490,6 +508,8 @@ moe_status_t run_gemm(moe_plan_t plan, GemmMode mode, const uint16_t* x, const i
     // gated and combining epilogues keep whole tiles (their column bookkeeping is per tile)
     prm.half_tiles = (glu || combine) ? 0 : plan->half_tiles;
     prm.nch = plan->scatter_parts;
+    prm.bg_head = (grouped || gather) ? 0 : bg_head_for(plan, out_cols);
+    if (prm.bg_head > 0) prm.nch = 1;  // the head is a prefix of experts: expert-major walk
     cudaError_t lerr;
     if (plan->pair) {
         lerr = launch_dispatch_gemm_pair(prm, plan->num_ctas, plan->smem, static_cast<cudaStream_t>(stream));

@@ -105,6 +105,9 @@ struct DispatchGemmParams {
     int half_tiles;                 // single CTAs: 0 whole tiles only; 1 every tile as two half-width
                                     //   tiles when the schedule has at most gridDim/2 tiles; 2 always
     int nch;                        // scatter order: parts per expert, chunk-major (nch E <= 1024)
+    int bg_head;                    // CTA pairs: > 0: every warp scatters only the rows of the first
+                                    //   experts holding at least bg_head pair tiles before the GEMM,
+                                    //   warp 3 the rest beside it (expert-major, nch 1); 0: all first
     int glu;                        // 1: W = [gate | up], each F = N/2 wide; out H, not Y
     int F;                          // N/2 when glu
     uint16_t* H;                    // glu: bf16 [S][F], silu(gate) * up
@@ -167,6 +170,15 @@ cudaError_t dispatch_gemm_prepare_attributes(int tile_n, int stages, size_t smem
 // ---------------------------------------------------------------- PTX helpers
 
 #if defined(__CUDACC__)
+
+// 16-byte read-only load that does not allocate in L1
+__device__ __forceinline__ uint4 ld_nc_na_v4(const uint4* ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

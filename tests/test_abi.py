@@ -43,15 +43,18 @@ def test_struct_layout_matches_header(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "moe.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(moe_shape_t),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(moe_shape_t),"
         " offsetof(moe_shape_t, timeout_ns), offsetof(moe_shape_t, debug_skip_publish),"
-        " sizeof(moe_plan_info_t), offsetof(moe_plan_info_t, workspace_bytes));return 0;}\n")
+        " sizeof(moe_plan_info_t), offsetof(moe_plan_info_t, workspace_bytes),"
+        " offsetof(moe_plan_info_t, half_tiles), offsetof(moe_plan_info_t, background_scatter));"
+        "return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
     vals = [int(v) for v in subprocess.check_output([str(exe)]).split()]
     assert vals == [ctypes.sizeof(binding.Shape), binding.Shape.timeout_ns.offset,
                     binding.Shape.debug_skip_publish.offset, ctypes.sizeof(binding.PlanInfo),
-                    binding.PlanInfo.workspace_bytes.offset]
+                    binding.PlanInfo.workspace_bytes.offset, binding.PlanInfo.half_tiles.offset,
+                    binding.PlanInfo.background_scatter.offset]
 
 
 def _plan_rc(lib, **kw):

@@ -25,6 +25,14 @@ def test_algorithmic_work_mixtral():
     assert flops / nbytes > 800
 
 
+def test_scatter_report_rate_only_without_background():
+    on = bench.scatter_report(100_000, 1e9, 6758.0, {"background_scatter": 152})
+    off = bench.scatter_report(100_000, 1e9, 6758.0, {"background_scatter": 0})
+    assert on["background"] and "frac_hbm" not in on
+    assert not off["background"] and abs(off["frac_hbm"] - 1e4 / 6758.0) < 1e-12
+    assert on["gbs"] == off["gbs"] == 1e4 and on["window_ms"] == 0.1
+
+
 def test_launches_per_step():
     assert bench.launches_per_step(workloads.WORKLOADS["mixtral"]) == 3
     assert bench.launches_per_step(workloads.WORKLOADS["decode"]) == 2

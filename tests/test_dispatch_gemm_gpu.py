@@ -315,6 +315,67 @@ def test_pair_mode_missing_flag_times_out():
     assert rc2 == 0, st2
 
 
+# Background scatter (CTA pairs, wide layers): every warp copies only the rows of the first
+# experts before the GEMM, warp 3 of every CTA the rest beside it.  MOE_BG_HEAD sets the head
+# (pair tiles) at plan time: 0 off; the automatic setting turns it on from 8192 columns.
+@pytest.mark.parametrize("head,kw", [
+    ("0", {}), ("1", {}), ("12", {}), (None, {}), ("100000", {}),
+    ("1", dict(producer_ctas=8)), ("1", dict(num_ctas=16, producer_ctas=4)),
+])
+def test_background_scatter_does_not_change_bits(head, kw, monkeypatch):
+    """Receive rows against the oracle, Y against the oracle and bit for bit against the
+    scatter-first run, and the fused combine bit for bit, for heads of one tile (the first
+    non-empty expert), several experts, every expert (no background copies) and under
+    role splits with fewer scatter CTAs and a small grid."""
+    wl = workloads.custom("pbg", 1500, 336, 8, 2, 512, 2, "zipf")  # 2 ranks, last k-block of 16
+    inp = workloads.make_inputs(wl, seed=31)
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    xb = workloads.bf16_bits(inp["x"])
+    rows = oracle.gather(xb, ref["perm"], wl.k)
+    x, W = inp["x"].cuda(), inp["W"].cuda()
+
+    def run(h):
+        if h is None:
+            monkeypatch.delenv("MOE_BG_HEAD", raising=False)
+        else:
+            monkeypatch.setenv("MOE_BG_HEAD", h)
+        plan, bufs, rc, status = run_path(wl, inp, tile_m=256, **kw)
+        assert rc == 0, status
+        assert plan.info["background_scatter"] == (0 if h is None else int(h))
+        check_recv(bufs, xb, ref, wl.k, wl.R, rows)
+        out = torch.full((wl.T, wl.N), float("nan"), device="cuda")
+        binding.dispatch_gemm_combine(plan, x, W, bufs, out)
+        rc, status = binding.moe_read_status(bufs.status)
+        assert rc == 0, status
+        check_recv(bufs, xb, ref, wl.k, wl.R, rows)
+        return bufs.Y.clone(), out
+
+    Y, out = run(head)
+    check_Y(Y.cpu().double().numpy(), oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"]))
+    Y0, out0 = run("0")
+    assert torch.equal(Y, Y0)
+    assert torch.equal(out, out0)
+
+
+def test_background_scatter_missing_flag_times_out(monkeypatch):
+    """A ready flag of a tile in the background range that never comes: the bounded wait
+    reports MOE_ERR_TIMEOUT with that tile, and the next call on the device is clean."""
+    monkeypatch.setenv("MOE_BG_HEAD", "1")
+    wl = workloads.custom("pbgfault", 600, 128, 2, 1, 256, 1, "none")
+    inp = workloads.make_inputs(wl, seed=10)
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    first_bg = int(-(-int(ref["counts"][0]) // 128))  # first 128-row tile of expert 1
+    assert first_bg > 0 and int(ref["counts"][1]) > 0
+    plan, bufs, rc, status = run_path(wl, inp, tile_m=256, timeout_ns=2_000_000,
+                                      debug_skip_publish=first_bg + 1)
+    assert plan.info["background_scatter"] == 1
+    assert rc == binding.MOE_ERR_TIMEOUT, status
+    assert status[1] == first_bg
+    monkeypatch.delenv("MOE_BG_HEAD")
+    plan2, bufs2, rc2, st2 = run_path(wl, inp)
+    assert rc2 == 0, st2
+
+
 @pytest.mark.parametrize("T,d,E,k,N,R", [
     (1024, 128, 1024, 8, 64, 32),   # the largest E and R the library accepts
     (200, 64, 64, 32, 32, 4),       # the largest k

@@ -110,6 +110,24 @@ def test_swiglu_up_pair_mode_512_wide_tiles(T, d, E, k, F):
     assert torch.equal(H[256].view(torch.int16), H[512].view(torch.int16))
 
 
+def test_swiglu_up_background_scatter_same_bits(monkeypatch):
+    """The gated up-projection on CTA pairs with the background scatter (head of one pair
+    tile): against the oracle, and H bit for bit against the scatter-first run."""
+    monkeypatch.setenv("MOE_BG_HEAD", "1")
+    plan = _up_check(1200, 128, 3, 2, 640, 1, "none", tile_m=256)
+    assert plan.info["background_scatter"] == 1
+    wl = workloads.custom("glu", 1200, 128, 3, 2, 1280, 1, "none")
+    inp = workloads.make_inputs(wl, seed=0, with_weights=False)
+    W1 = workloads.make_ffn_weights(wl, 640, seed=0)[0].cuda()
+    H = {}
+    for head in ("1", "0"):
+        monkeypatch.setenv("MOE_BG_HEAD", head)
+        _, bufs, rc, status = _run_up(wl, 640, inp, W1, tile_m=256)
+        assert rc == 0, status
+        H[head] = bufs.H.clone()
+    assert torch.equal(H["1"].view(torch.int16), H["0"].view(torch.int16))
+
+
 def test_swiglu_rejects_192_wide_tiles():
     wl = workloads.custom("g192", 100, 64, 4, 2, 384)
     plan = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, tile_n=192)
