@@ -882,6 +882,15 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     const bool split = p.half_tiles == 2 || (p.half_tiles == 1 && 2u * total_tiles <= gridDim.x);
     const uint32_t split_from = split ? 0u : total_tiles;
     const uint32_t total_claims = 2u * total_tiles - split_from;
+    // a schedule of 2-8 waves of claims: only as many CTAs claim as fill every wave (the
+    // others leave after their scatter share), so that an HBM-bound layer's CTAs end
+    // together instead of a partial last wave running on a few of them
+    bool claims = true;
+    {
+        const uint32_t g = gridDim.x;
+        const uint32_t waves = (total_claims + g - 1) / g;
+        if (waves >= 2 && waves <= 8) claims = (uint32_t)ctl->role < (total_claims + waves - 1) / waves;
+    }
     const int e_per_rank = p.E / p.R;
     tma_prefetch_map(&p.b_map);
     if (!p.gather)  // no A tensor map in the gather mode
@@ -897,7 +906,7 @@ __device__ void tma_role(const DispatchGemmParams& p, SmemCtl* ctl, const int* m
     // claim a tile, describe it, hand it to the MMA and epilogue warps, read its flag
     auto push_next = [&](TileInfo& ti, uint32_t& flag) -> bool {
         if (!wait_bar(smem_addr(&ctl->sempty[slot]), sphase ^ 1u, w, 1)) return false;
-        const uint32_t claim = atomicAdd(p.hdr + kHdrTileCtr, 1u);
+        const uint32_t claim = claims ? atomicAdd(p.hdr + kHdrTileCtr, 1u) : total_claims;
         if (claim >= total_claims) {
             ti.e = ti.m = ti.n = ti.mtile = ti.row0 = ti.rank = ti.arow = ti.m128 = ti.half = 0;
             ti.rows = -1;
