@@ -315,6 +315,26 @@ def test_pair_mode_missing_flag_times_out():
     assert rc2 == 0, st2
 
 
+def test_even_waves_same_bits():
+    """A single-CTA schedule of about four waves of tiles: only as many CTAs claim as fill
+    every wave.  Against the oracle, and bit for bit against a 16-CTA grid (40 waves, where
+    every CTA claims)."""
+    wl = workloads.custom("waves", 4096, 128, 16, 2, 1024, 1, "zipf")
+    inp = workloads.make_inputs(wl, seed=33)
+    outs = []
+    for kw in (dict(), dict(num_ctas=16)):
+        plan, bufs, rc, status = run_path(wl, inp, tile_m=128, tile_n=128, **kw)
+        assert rc == 0, status
+        outs.append(bufs.Y.clone())
+    tiles = int(((bufs.counts.cpu() + 127) // 128).sum()) * (wl.N // 128)
+    grid = binding.moe_plan(wl.T, wl.d, wl.E, wl.k, wl.N, tile_m=128, tile_n=128).info["num_ctas"]
+    assert 2 * grid < tiles <= 8 * grid  # the default grid runs the even-waves rule
+    assert torch.equal(outs[0], outs[1])
+    ref = oracle.route(inp["logits"].numpy(), wl.k)
+    rows = oracle.gather(workloads.bf16_bits(inp["x"]), ref["perm"], wl.k)
+    check_Y(outs[0].cpu().double().numpy(), oracle.grouped_gemm(rows, workloads.bf16_bits(inp["W"]), ref["offsets"]))
+
+
 # Background scatter (CTA pairs, wide layers): every warp copies only the rows of the first
 # experts before the GEMM, warp 3 of every CTA the rest beside it.  MOE_BG_HEAD sets the head
 # (pair tiles) at plan time: 0 off; the automatic setting turns it on from 8192 columns.
