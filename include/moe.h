@@ -148,6 +148,13 @@ typedef struct moe_plan_info {
  *                         after any device error status); the calls return
  *                         their counters to zero themselves.
  * Host only (queries device attributes); launches nothing.
+ * Tuning overrides read from the environment when the plan is built (for sweeps
+ * and tests; none changes a result bit, and unset is the default schedule):
+ *   MOE_HALF_TILES=0|2     single-CTA plans: never / always split tiles in halves
+ *   MOE_BG_HEAD=n          CTA-pair plans: pair tiles the all-warps scatter covers
+ *                          before the GEMM (0: the whole scatter first)
+ *   MOE_SCATTER_PARTS=p    the scatter's parts per expert (1: expert-major)
+ *   MOE_TILE_BAND=b        row tiles per schedule band (0: the whole expert)
  */
 MOE_API moe_status_t moe_plan(const moe_shape_t* shape, int device, moe_plan_t* plan,
                       size_t* workspace_bytes);
