@@ -43,8 +43,10 @@ def _case(i: int) -> dict:
     else:
         tile_n = 0
     out_dtype = binding.MOE_OUT_BF16 if rng.random() < 0.25 else binding.MOE_OUT_F32
+    # CTA pairs: the background scatter's head (pair tiles), or the automatic setting
+    bg_head = str(rng.choice(["auto", "0", "1", "4", "16"]))
     return dict(T=T, d=d, E=E, k=k, N=N, R=R, bias=bias, tile_m=tile_m, tile_n=tile_n,
-                out_dtype=out_dtype)
+                out_dtype=out_dtype, bg_head=bg_head)
 
 
 def _check_bf16(Y_bf16: np.ndarray, Yref: np.ndarray):
@@ -62,8 +64,12 @@ def _check_out(Y_dev: torch.Tensor, Yref: np.ndarray, bf16: bool):
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
-def test_random_shapes_every_entry_point(i):
+def test_random_shapes_every_entry_point(i, monkeypatch):
     c = _case(i)
+    if c["bg_head"] == "auto":
+        monkeypatch.delenv("MOE_BG_HEAD", raising=False)
+    else:
+        monkeypatch.setenv("MOE_BG_HEAD", c["bg_head"])
     wl = workloads.custom("fuzz", c["T"], c["d"], c["E"], c["k"], c["N"], c["R"], c["bias"])
     inp = workloads.make_inputs(wl, seed=100 + i)
     bf16 = c["out_dtype"] == binding.MOE_OUT_BF16
